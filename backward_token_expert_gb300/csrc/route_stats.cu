@@ -1,0 +1,395 @@
+// Step 1 of the path: routing statistics, capacity, drop rate and retention
+// quotas ("Expert Parallel Math Deep": importance P_e, load f_e, the
+// auxiliary loss E * sum f_e P_e, capacity C = CF * T k / E and the drop
+// rate; LRMoE sec. 3.1 and Alg. 1 line 1: routed counts n_e and quotas
+// 0 <= Q_e <= n_e), plus the stable expert bucket and prefix offsets that
+// selection and compaction consume (LRMoE sec. 3.3).
+//
+// Three launches:
+//   rs_count    one block per contiguous chunk of tokens: per-block expert
+//               histogram (shared-memory atomics) and per-block partial sums
+//               of the softmax (one warp per token, fixed reduction order);
+//   rs_finalize one block: counts, offsets, per-(expert, block) bucket bases,
+//               P, f, quotas and the summary;
+//   rs_scatter  same chunking as rs_count: stable scatter of pair ids into
+//               the bucket (each warp owns a contiguous sub-range, ranks
+//               inside a warp come from __match_any_sync).
+#include <limits.h>
+#include <math.h>
+
+#include "lrm_internal.cuh"
+
+namespace lrm {
+
+namespace {
+
+constexpr int RS_THREADS = 256;
+constexpr int RS_WARPS = RS_THREADS / 32;
+constexpr int RS_PAIRS_PER_BLOCK = 1024;
+constexpr int RS_FIN_THREADS = 1024;
+
+struct RsLayout {
+  int tpb;    // tokens per block
+  int nblk;   // blocks of rs_count / rs_scatter
+  size_t hist_off, p_off, bytes;
+};
+
+RsLayout rs_layout(const lrm_dims& d) {
+  RsLayout L;
+  L.tpb = RS_PAIRS_PER_BLOCK / d.k;
+  if (L.tpb < 1) L.tpb = 1;
+  L.nblk = (d.T + L.tpb - 1) / L.tpb;
+  const size_t cells = static_cast<size_t>(L.nblk) * d.E;
+  L.hist_off = 0;
+  L.p_off = ((cells * sizeof(int32_t) + 255) / 256) * 256;
+  L.bytes = L.p_off + cells * sizeof(float);
+  return L;
+}
+
+// A pair is valid when its expert id is in range and differs from the ids
+// of the earlier slots of the same token.
+__device__ __forceinline__ bool pair_valid(const int32_t* __restrict__ idx, int p, int k, int E, int e) {
+  if (e < 0 || e >= E) return false;
+  const int t0 = p - (p % k);
+  for (int q = t0; q < p; ++q)
+    if (__ldg(idx + q) == e) return false;
+  return true;
+}
+
+__global__ void __launch_bounds__(RS_THREADS) rs_count(const float* __restrict__ logits,
+                                                       const int32_t* __restrict__ idx, int T, int E, int k,
+                                                       int tpb, int nblk, int32_t* __restrict__ ws_hist,
+                                                       float* __restrict__ ws_p, unsigned int* status) {
+  extern __shared__ float rs_smem[];
+  float* pw = rs_smem;                                            // [RS_WARPS][E]
+  int* hist = reinterpret_cast<int*>(rs_smem + RS_WARPS * E);     // [E]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  for (int i = tid; i < RS_WARPS * E; i += RS_THREADS) pw[i] = 0.f;
+  for (int i = tid; i < E; i += RS_THREADS) hist[i] = 0;
+  __syncthreads();
+
+  const int tok0 = blockIdx.x * tpb;
+  const int tok1 = min(T, tok0 + tpb);
+  bool bad = false;
+  for (int p = tok0 * k + tid; p < tok1 * k; p += RS_THREADS) {
+    const int e = __ldg(idx + p);
+    if (pair_valid(idx, p, k, E, e))
+      atomicAdd(&hist[e], 1);
+    else
+      bad = true;
+  }
+  if (bad) raise_flag(status, LRM_ERR_INDEX);
+
+  // softmax over all E experts, one warp per token; lane owns experts lane + 32 i
+  float* mine = pw + warp * E;
+  for (int t = tok0 + warp; t < tok1; t += RS_WARPS) {
+    const float* row = logits + static_cast<size_t>(t) * E;
+    float v[32];
+    float mx = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int e = lane + 32 * i;
+      v[i] = (e < E) ? __ldg(row + e) : -INFINITY;
+      mx = fmaxf(mx, v[i]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int e = lane + 32 * i;
+      v[i] = (e < E) ? expf(v[i] - mx) : 0.f;
+      s += v[i];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E) mine[e] += v[i] / s;
+    }
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += RS_THREADS) {
+    float acc = 0.f;
+#pragma unroll
+    for (int w = 0; w < RS_WARPS; ++w) acc += pw[w * E + e];
+    ws_p[static_cast<size_t>(e) * nblk + blockIdx.x] = acc;
+    ws_hist[static_cast<size_t>(e) * nblk + blockIdx.x] = hist[e];
+  }
+}
+
+// Block-wide exclusive scan of one int per thread (blockDim = 1024).
+__device__ int block_exclusive_scan_1024(int v, int* s_warp, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s_warp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = s_warp[lane];
+    int z = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, z, o);
+      if (lane >= o) z += y;
+    }
+    s_warp[lane] = z - w;
+    if (lane == 31) *total = z;
+  }
+  __syncthreads();
+  const int r = s_warp[warp] + x - v;
+  __syncthreads();
+  return r;
+}
+
+__global__ void __launch_bounds__(RS_FIN_THREADS) rs_finalize(
+    int T, int E, int k, int nblk, int32_t cf_num, int32_t cf_den, int32_t rho_num, int32_t rho_den,
+    int32_t* __restrict__ ws_hist, const float* __restrict__ ws_p, int32_t* __restrict__ counts,
+    int32_t* __restrict__ offsets, float* __restrict__ P, float* __restrict__ f, int32_t* __restrict__ quota,
+    lrm_route_summary* __restrict__ summary) {
+  __shared__ int s_warp[32];
+  __shared__ int s_total;
+  __shared__ int s_cnt[1024];
+  __shared__ int s_off[1024];
+  __shared__ double s_P[1024];
+  __shared__ long long s_red_i[6][32];
+  __shared__ double s_red_d[2][32];
+  const int e = threadIdx.x;
+  const int lane = e & 31, warp = e >> 5;
+  const bool live = e < E;
+  const long long N = static_cast<long long>(T) * k;
+
+  // phase 1: one warp per expert row (expert-major workspace, coalesced)
+  for (int x = warp; x < E; x += RS_FIN_THREADS / 32) {
+    const size_t row = static_cast<size_t>(x) * nblk;
+    int c = 0;
+    double ps = 0.0;
+    for (int b = lane; b < nblk; b += 32) {
+      c += ws_hist[row + b];
+      ps += static_cast<double>(ws_p[row + b]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      c += __shfl_xor_sync(0xffffffffu, c, o);
+      ps += __shfl_xor_sync(0xffffffffu, ps, o);
+    }
+    if (lane == 0) {
+      s_cnt[x] = c;
+      s_P[x] = ps;
+    }
+  }
+  __syncthreads();
+  const int cnt = live ? s_cnt[e] : 0;
+  const int off = block_exclusive_scan_1024(cnt, s_warp, &s_total);
+  if (live) {
+    counts[e] = cnt;
+    offsets[e] = off;
+    s_off[e] = off;
+  }
+  if (e == 0) offsets[E] = s_total;
+  __syncthreads();
+  // phase 2: per-(expert, block) base offsets of the stable scatter, in place
+  for (int x = warp; x < E; x += RS_FIN_THREADS / 32) {
+    const size_t row = static_cast<size_t>(x) * nblk;
+    int run = s_off[x];
+    for (int c0 = 0; c0 < nblk; c0 += 32) {
+      const int b = c0 + lane;
+      const int v = b < nblk ? ws_hist[row + b] : 0;
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (b < nblk) ws_hist[row + b] = run + incl - v;
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+  }
+
+  // capacity and quota in exact integer arithmetic
+  const long long C = (static_cast<long long>(cf_num) * N) / (static_cast<long long>(cf_den) * E);
+  double Pe = 0.0;
+  long long q = 0, drop = 0;
+  if (live) {
+    Pe = (T > 0) ? s_P[e] / T : 0.0;
+    const long long m = cnt < C ? cnt : C;
+    q = (static_cast<long long>(rho_num) * m + rho_den - 1) / rho_den;
+    drop = cnt > C ? cnt - C : 0;
+    P[e] = static_cast<float>(Pe);
+    f[e] = N > 0 ? static_cast<float>(static_cast<double>(cnt) / static_cast<double>(N)) : 0.f;
+    quota[e] = static_cast<int32_t>(q);
+  }
+  const double fe = (live && N > 0) ? static_cast<double>(cnt) / static_cast<double>(N) : 0.0;
+
+  // deterministic block reductions
+  long long vi[6] = {drop, q, live ? cnt : LLONG_MIN, live ? cnt : LLONG_MAX, (live && cnt > 0) ? 1 : 0, 0};
+  double vd[2] = {fe * Pe, Pe};
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    vi[0] += __shfl_xor_sync(0xffffffffu, vi[0], o);
+    vi[1] += __shfl_xor_sync(0xffffffffu, vi[1], o);
+    vi[2] = max(vi[2], __shfl_xor_sync(0xffffffffu, vi[2], o));
+    vi[3] = min(vi[3], __shfl_xor_sync(0xffffffffu, vi[3], o));
+    vi[4] += __shfl_xor_sync(0xffffffffu, vi[4], o);
+    vd[0] += __shfl_xor_sync(0xffffffffu, vd[0], o);
+    vd[1] += __shfl_xor_sync(0xffffffffu, vd[1], o);
+  }
+  if (lane == 0) {
+    for (int i = 0; i < 5; ++i) s_red_i[i][warp] = vi[i];
+    s_red_d[0][warp] = vd[0];
+    s_red_d[1][warp] = vd[1];
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = blockDim.x >> 5;
+    long long a0 = lane < nw ? s_red_i[0][lane] : 0, a1 = lane < nw ? s_red_i[1][lane] : 0;
+    long long a2 = lane < nw ? s_red_i[2][lane] : LLONG_MIN, a3 = lane < nw ? s_red_i[3][lane] : LLONG_MAX;
+    long long a4 = lane < nw ? s_red_i[4][lane] : 0;
+    double d0 = lane < nw ? s_red_d[0][lane] : 0.0, d1 = lane < nw ? s_red_d[1][lane] : 0.0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      a0 += __shfl_xor_sync(0xffffffffu, a0, o);
+      a1 += __shfl_xor_sync(0xffffffffu, a1, o);
+      a2 = max(a2, __shfl_xor_sync(0xffffffffu, a2, o));
+      a3 = min(a3, __shfl_xor_sync(0xffffffffu, a3, o));
+      a4 += __shfl_xor_sync(0xffffffffu, a4, o);
+      d0 += __shfl_xor_sync(0xffffffffu, d0, o);
+      d1 += __shfl_xor_sync(0xffffffffu, d1, o);
+    }
+    if (lane == 0) {
+      lrm_route_summary s;
+      s.N = static_cast<int32_t>(N);
+      s.C = static_cast<int32_t>(C);
+      s.slots = static_cast<int32_t>(C * E);
+      s.dropped = static_cast<int32_t>(a0);
+      s.retained = static_cast<int32_t>(a1);
+      s.max_count = static_cast<int32_t>(a2);
+      s.min_count = static_cast<int32_t>(a3);
+      s.nonempty = static_cast<int32_t>(a4);
+      s.aux_unscaled = static_cast<float>(E * d0);
+      s.drop_rate = N > 0 ? static_cast<float>(static_cast<double>(a0) / static_cast<double>(N)) : 0.f;
+      s.util = C > 0 ? static_cast<float>(static_cast<double>(N - a0) / static_cast<double>(C * E)) : 0.f;
+      s.rho_real = N > 0 ? static_cast<float>(static_cast<double>(a1) / static_cast<double>(N)) : 0.f;
+      s.max_over_mean =
+          N > 0 ? static_cast<float>(static_cast<double>(a2) * E / static_cast<double>(N)) : 0.f;
+      s.sum_P = static_cast<float>(d1);
+      *summary = s;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(RS_THREADS) rs_scatter(const int32_t* __restrict__ idx, int T, int E, int k,
+                                                         int tpb, int nblk, const int32_t* __restrict__ ws_base,
+                                                         int32_t* __restrict__ bucket) {
+  extern __shared__ int rs_cnt[];  // [RS_WARPS][E]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  for (int i = tid; i < RS_WARPS * E; i += RS_THREADS) rs_cnt[i] = 0;
+  __syncthreads();
+  const int p0 = blockIdx.x * tpb * k;
+  const int p1 = min(T, (blockIdx.x + 1) * tpb) * k;
+  const int span = (p1 - p0 + RS_WARPS - 1) / RS_WARPS;
+  const int w0 = min(p1, p0 + warp * span);
+  const int w1 = min(p1, w0 + span);
+  int* mine = rs_cnt + warp * E;
+  const unsigned lt_mask = (1u << lane) - 1u;
+
+  // pass A: per-warp histogram of its contiguous sub-range
+  for (int base = w0; base < w1; base += 32) {
+    const int p = base + lane;
+    int e = -1;
+    if (p < w1) {
+      const int v = __ldg(idx + p);
+      if (pair_valid(idx, p, k, E, v)) e = v;
+    }
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    if (e >= 0 && (peers & lt_mask) == 0) mine[e] += __popc(peers);
+    __syncwarp();
+  }
+  __syncthreads();
+  // per expert: the block's base offset, then exclusive prefix over the warps
+  for (int e = tid; e < E; e += RS_THREADS) {
+    int run = ws_base[static_cast<size_t>(e) * nblk + blockIdx.x];
+#pragma unroll
+    for (int w = 0; w < RS_WARPS; ++w) {
+      const int c = rs_cnt[w * E + e];
+      rs_cnt[w * E + e] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  // pass B: stable placement, ascending pair index within every expert
+  for (int base = w0; base < w1; base += 32) {
+    const int p = base + lane;
+    int e = -1;
+    if (p < w1) {
+      const int v = __ldg(idx + p);
+      if (pair_valid(idx, p, k, E, v)) e = v;
+    }
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    int pos = 0;
+    if (e >= 0) pos = mine[e] + __popc(peers & lt_mask);
+    __syncwarp();
+    if (e >= 0) {
+      bucket[pos] = p;
+      if ((peers & lt_mask) == 0) mine[e] += __popc(peers);
+    }
+    __syncwarp();
+  }
+}
+
+}  // namespace
+
+size_t route_stats_workspace_bytes(const lrm_dims& d) { return rs_layout(d).bytes; }
+
+}  // namespace lrm
+
+using namespace lrm;
+
+extern "C" lrm_status lrm_route_stats(lrm_ctx* ctx, const float* logits, const int32_t* expert_idx, lrm_dims dims,
+                                      int32_t cf_num, int32_t cf_den, int32_t rho_num, int32_t rho_den,
+                                      int32_t* counts, int32_t* offsets, int32_t* bucket, float* P, float* f,
+                                      int32_t* quota, lrm_route_summary* summary, void* ws, size_t ws_bytes,
+                                      void* stream) {
+  if (ctx == nullptr) return LRM_ERR_INVALID_ARG;
+  lrm_status st = check_dims(dims);
+  if (st != LRM_OK) return st;
+  if (cf_num <= 0 || cf_den <= 0 || rho_den <= 0 || rho_num < 0 || rho_num > rho_den)
+    return LRM_ERR_INVALID_ARG;
+  if (counts == nullptr || offsets == nullptr || P == nullptr || f == nullptr || quota == nullptr ||
+      summary == nullptr)
+    return LRM_ERR_INVALID_ARG;
+  if (dims.T > 0 && (logits == nullptr || expert_idx == nullptr || bucket == nullptr))
+    return LRM_ERR_INVALID_ARG;
+  const void* ptrs[] = {logits, expert_idx, counts, offsets, bucket, P, f, quota, summary, ws};
+  for (const void* p : ptrs)
+    if (p != nullptr && !aligned(p, 4)) return LRM_ERR_ALIGN;
+  const RsLayout L = rs_layout(dims);
+  if (L.nblk > 0 && (ws == nullptr || ws_bytes < L.bytes)) return LRM_ERR_WORKSPACE;
+  if (!aligned(ws, 256)) return LRM_ERR_ALIGN;
+  DeviceGuard guard(ctx->device);
+  if (!guard.ok) return LRM_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t* ws_hist = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + L.hist_off);
+  float* ws_p = reinterpret_cast<float*>(static_cast<char*>(ws) + L.p_off);
+  if (L.nblk > 0) {
+    const size_t smem1 = (RS_WARPS + 1) * dims.E * sizeof(float);
+    rs_count<<<L.nblk, RS_THREADS, smem1, s>>>(logits, expert_idx, dims.T, dims.E, dims.k, L.tpb, L.nblk,
+                                               ws_hist, ws_p, ctx->d_status);
+    if ((st = launch_status()) != LRM_OK) return st;
+  }
+  rs_finalize<<<1, RS_FIN_THREADS, 0, s>>>(dims.T, dims.E, dims.k, L.nblk, cf_num, cf_den, rho_num, rho_den,
+                                           ws_hist, ws_p, counts, offsets, P, f, quota, summary);
+  if ((st = launch_status()) != LRM_OK) return st;
+  if (L.nblk > 0) {
+    const size_t smem3 = RS_WARPS * dims.E * sizeof(int);
+    rs_scatter<<<L.nblk, RS_THREADS, smem3, s>>>(expert_idx, dims.T, dims.E, dims.k, L.tpb, L.nblk, ws_hist,
+                                                 bucket);
+    if ((st = launch_status()) != LRM_OK) return st;
+  }
+  return LRM_OK;
+}

@@ -1,0 +1,181 @@
+"""One backward recalibration of an MoE layer's FC2 through the C ABI.
+
+``Recalibration`` owns the device buffers of one layer shape (allocated once
+with torch, which is used here only for device memory and streams) and
+enqueues the six library calls of the path on one stream, with no host
+synchronisation in between:
+
+    lrm_route_stats -> lrm_score -> lrm_select -> lrm_compact
+                    -> lrm_grouped_dgrad -> lrm_grouped_wgrad
+
+(LRMoE Alg. 1 lines 1 and 13-17; the input-gradient product runs before the
+weight-gradient product, the order TopoEP sec. 3.3 schedules them in).
+"""
+
+from __future__ import annotations
+
+import dataclasses
+from fractions import Fraction
+
+import torch
+
+from . import lrm as L
+
+
+def capacity(N: int, E: int, cf: Fraction) -> int:
+    """C = floor(CF * N / E) in exact rational arithmetic."""
+    cf = Fraction(cf)
+    return (cf.numerator * N) // (cf.denominator * E)
+
+
+def max_retained_rows(T: int, E: int, k: int, cf: Fraction, rho: Fraction) -> int:
+    """Host upper bound of sum_e ceil(rho * min(n_e, C)) over any routing.
+
+    Each quota is at most ceil(rho * C) and at most n_e, so the total is at
+    most min(N, E * ceil(rho * C)).
+    """
+    N = T * k
+    C = capacity(N, E, cf)
+    rho = Fraction(rho)
+    per = -((-rho.numerator * C) // rho.denominator)
+    return max(0, min(N, E * per))
+
+
+@dataclasses.dataclass
+class Buffers:
+    counts: torch.Tensor
+    offsets: torch.Tensor
+    bucket: torch.Tensor
+    P: torch.Tensor
+    f: torch.Tensor
+    quota: torch.Tensor
+    summary: torch.Tensor
+    ws_route: torch.Tensor
+    score: torch.Tensor
+    sel_offsets: torch.Tensor
+    sel_ids: torch.Tensor
+    delta_c: torch.Tensor
+    phi_c: torch.Tensor
+    alpha_c: torch.Tensor
+    dphi_c: torch.Tensor
+    dW: torch.Tensor
+
+
+class Recalibration:
+    """Device buffers plus the library calls of one recalibration step."""
+
+    def __init__(self, T, E, k, h, I, cf=Fraction(5, 4), rho=Fraction(3, 4), device=0, max_rows=None):
+        self.T, self.E, self.k, self.h, self.I = int(T), int(E), int(k), int(h), int(I)
+        self.N = self.T * self.k
+        self.cf = Fraction(cf)
+        self.rho = Fraction(rho)
+        self.device = torch.device("cuda", device) if isinstance(device, int) else torch.device(device)
+        self.dims = L.dims_of(T, E, k, h, I)
+        self.ctx = L.lrm_create(self.device.index or 0)
+        self.C = capacity(self.N, self.E, self.cf)
+        self.max_rows = max_retained_rows(T, E, k, self.cf, self.rho) if max_rows is None else int(max_rows)
+        dev = self.device
+        ws_bytes = L.lrm_workspace_size(self.ctx, L.LRM_OP_ROUTE_STATS, self.dims)
+        i32 = dict(dtype=torch.int32, device=dev)
+        f32 = dict(dtype=torch.float32, device=dev)
+        bf = dict(dtype=torch.bfloat16, device=dev)
+        R = max(1, self.max_rows)
+        self.buf = Buffers(
+            counts=torch.empty(E, **i32),
+            offsets=torch.empty(E + 1, **i32),
+            bucket=torch.empty(max(1, self.N), **i32),
+            P=torch.empty(E, **f32),
+            f=torch.empty(E, **f32),
+            quota=torch.empty(E, **i32),
+            summary=torch.zeros(L.SUMMARY_BYTES, dtype=torch.uint8, device=dev),
+            ws_route=torch.empty(max(256, ws_bytes), dtype=torch.uint8, device=dev),
+            score=torch.empty(max(1, self.N), **f32),
+            sel_offsets=torch.empty(E + 1, **i32),
+            sel_ids=torch.empty(R, **i32),
+            delta_c=torch.empty(R, h, **bf),
+            phi_c=torch.empty(R, I, **bf),
+            alpha_c=torch.empty(R, **f32),
+            dphi_c=torch.empty(R, I, **bf),
+            dW=torch.empty(E, h, I, **f32),
+        )
+        self.ws_bytes = self.buf.ws_route.numel()
+
+    def close(self):
+        if getattr(self, "ctx", None):
+            L.lrm_destroy(self.ctx)
+            self.ctx = None
+
+    def __del__(self):  # pragma: no cover - best effort
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # -- the steps -----------------------------------------------------------
+
+    def route_stats(self, logits, expert_idx, stream=None, quota_override=None):
+        b = self.buf
+        L.lrm_route_stats(self.ctx, logits, expert_idx, self.dims, self.cf, self.rho, b.counts, b.offsets,
+                          b.bucket, b.P, b.f, b.quota, b.summary, b.ws_route, self.ws_bytes, stream)
+        if quota_override is not None:
+            b.quota.copy_(quota_override)
+
+    def score(self, g, phi, alpha, stream=None):
+        L.lrm_score(self.ctx, g, phi, alpha, self.dims, self.buf.score, stream)
+
+    def select(self, stream=None, score=None):
+        b = self.buf
+        L.lrm_select(self.ctx, b.score if score is None else score, b.offsets, b.bucket, b.quota, self.dims,
+                     self.max_rows, b.sel_offsets, b.sel_ids, None, 0, stream)
+
+    def compact(self, g, phi, alpha, stream=None):
+        b = self.buf
+        L.lrm_compact(self.ctx, g, phi, alpha, b.sel_offsets, b.sel_ids, self.dims, self.max_rows, b.delta_c,
+                      b.phi_c, b.alpha_c, stream)
+
+    def dgrad(self, W, stream=None):
+        b = self.buf
+        L.lrm_grouped_dgrad(self.ctx, b.delta_c, W, b.sel_offsets, self.dims, self.max_rows, b.dphi_c, stream)
+
+    def wgrad(self, stream=None, accumulate=0):
+        b = self.buf
+        L.lrm_grouped_wgrad(self.ctx, b.delta_c, b.phi_c, b.sel_offsets, self.dims, self.max_rows, accumulate,
+                            b.dW, stream)
+
+    def backward_steps(self, g, phi, alpha, W, stream=None):
+        """score -> select -> compact -> dgrad -> wgrad (quotas already set)."""
+        self.score(g, phi, alpha, stream)
+        self.select(stream)
+        self.compact(g, phi, alpha, stream)
+        self.dgrad(W, stream)
+        self.wgrad(stream)
+
+    def run(self, logits, expert_idx, g, phi, alpha, W, stream=None):
+        """The whole path, enqueued on one stream."""
+        self.route_stats(logits, expert_idx, stream)
+        self.backward_steps(g, phi, alpha, W, stream)
+
+    def summary(self) -> dict:
+        raw = bytes(self.buf.summary.cpu().numpy().tobytes())
+        s = L.RouteSummary.from_buffer_copy(raw)
+        return {name: getattr(s, name) for name, _ in L.RouteSummary._fields_}
+
+    def device_status(self, stream=None) -> int:
+        return L.lrm_get_device_status(self.ctx, stream)
+
+
+def to_device_inputs(inp, device="cuda"):
+    """Copy a workloads.Inputs record to device tensors (bf16 bits viewed as bf16)."""
+    import numpy as np
+
+    def bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
+
+    return dict(
+        logits=torch.from_numpy(inp.logits).to(device),
+        expert_idx=torch.from_numpy(inp.expert_idx).to(device),
+        alpha=torch.from_numpy(inp.alpha).to(device),
+        g=bf(inp.g),
+        phi=bf(inp.phi),
+        W=bf(inp.W),
+    )

@@ -1,0 +1,521 @@
+"""Throughput of LRMoE's backward recalibration path on GB300.
+
+One step = one pass of the whole path over one layer batch, through the C
+ABI: route stats -> LRM score -> per-expert top-Q select -> compaction ->
+grouped dgrad -> grouped wgrad.  The metric is retained token-expert pairs per
+second (sum of the quotas over the step time).  Inputs are seeded synthetic
+tensors shaped like a Qwen3-30B-A3B MoE layer (T=32768, E=128, k=8, h=2048,
+I=768, bf16) unless --workload names another one; they are resident in HBM
+and larger than L2, so no L2 flush is done between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle (the path's correctness
+reference) on the host cores, on a bounded token slice of the same workload.
+Under torchrun every rank runs an independent replica of the layer (the path
+has no data exchange); rank 0 prints one JSON line.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "qwen3_30b_a3b_T32768_E128_k8_h2048_I768"
+METRIC = "retained pairs/s through score->select->compact->grouped GEMM"
+UNIT = "pairs/s"
+KERNELS = ("route_stats", "score", "select", "compact", "dgrad", "wgrad")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-comparator", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--ref-tokens", type=int, default=0, help="token slice of the reference arm's step")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            p = json.load(fh)
+        return dict(hbm=float(p["hbm_gbs"]), bf16=float(p["bf16_tflops"]),
+                    bf16_sustained=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), source="measured")
+    except (OSError, KeyError, ValueError):
+        return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def _snapshot(self):
+        try:
+            out = subprocess.run(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                  "--format=csv,noheader,nounits"], capture_output=True, text=True, timeout=10)
+            for line in out.stdout.strip().splitlines():
+                self.rows.append([x.strip() for x in line.split(",")])
+        except (OSError, subprocess.SubprocessError):
+            pass
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+
+        def reader():
+            for line in self.proc.stdout:
+                self.rows.append([x.strip() for x in line.split(",")])
+
+        self.thread = threading.Thread(target=reader, daemon=True)
+        self.thread.start()
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self.thread is not None:
+                self.thread.join(timeout=5)
+        if not self.rows:
+            self._snapshot()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in self.rows:
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work per launch (bytes or flop)
+
+
+def algorithmic_work(w, retained):
+    T, E, k, h, I = w.T, w.E, w.k, w.h, w.I
+    N = T * k
+    return {
+        "route_stats": ("hbm", T * (4 * E + 4 * k) + 4 * N),
+        "score": ("hbm", 2 * T * h + N * (2 * I + 8)),
+        "select": ("hbm", 8 * N + 4 * retained),
+        "compact": ("hbm", retained * (4 * (h + I) + 8)),
+        "dgrad": ("tensor", 2 * retained * h * I),
+        "wgrad": ("tensor", 2 * retained * h * I),
+    }
+
+
+def roofline_entry(kind, work, ms, pk, sustained):
+    if kind == "hbm":
+        achieved = work / (ms * 1e-3) / 1e9
+        peak = pk["hbm"]
+        unit = "GB/s"
+    else:
+        achieved = work / (ms * 1e-3) / 1e12
+        peak = pk["bf16_sustained"] if sustained else pk["bf16"]
+        unit = "TFLOP/s"
+    return {"bound": kind, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+            "frac": round(achieved / peak, 4)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+
+
+def run_ours(args, rank, world, local):
+    import torch
+
+    from backward_token_expert_gb300 import build as B
+    from backward_token_expert_gb300.pipeline import Recalibration, to_device_inputs
+    from workloads import generate, get_workload
+
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    if rank == 0:
+        B.build()
+    if dist:
+        dist.barrier()
+
+    # independent replicas: rank r draws its own layer batch (seed r)
+    w = get_workload(args.workload, seed=rank)
+    inp = generate(w)
+    rec = Recalibration(w.T, w.E, w.k, w.h, w.I, w.cf, w.rho, device=local)
+    d = to_device_inputs(inp, f"cuda:{local}")
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev is None:
+            rec.run(d["logits"], d["expert_idx"], d["g"], d["phi"], d["alpha"], d["W"])
+            return
+        ev[0].record(stream)
+        rec.route_stats(d["logits"], d["expert_idx"])
+        ev[1].record(stream)
+        rec.score(d["g"], d["phi"], d["alpha"])
+        ev[2].record(stream)
+        rec.select()
+        ev[3].record(stream)
+        rec.compact(d["g"], d["phi"], d["alpha"])
+        ev[4].record(stream)
+        rec.dgrad(d["W"])
+        ev[5].record(stream)
+        rec.wgrad()
+        ev[6].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    flags = rec.device_status()
+    if flags:
+        raise RuntimeError(f"device status flags {flags:#x}")
+    summ = rec.summary()
+    retained = int(summ["retained"])
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(K)]
+    sampler = ClockSampler(local) if rank == 0 else None
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    t_host0 = time.perf_counter()
+    for i in range(K):
+        step(evs[i])
+    torch.cuda.synchronize()
+    t_host = time.perf_counter() - t_host0
+    if sampler:
+        sampler.stop()
+    if dist:
+        dist.barrier()
+    total_ms = evs[0][0].elapsed_time(evs[-1][6])
+    per = {name: [evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K)] for j, name in enumerate(KERNELS)}
+    if dist:
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    flags = rec.device_status()
+    if flags:
+        raise RuntimeError(f"device status flags {flags:#x} after the timed steps")
+
+    result = None
+    if rank == 0:
+        pk = peaks()
+        work = algorithmic_work(w, retained)
+        kernels = {}
+        for name in KERNELS:
+            ms = statistics.mean(per[name])
+            kind, wk = work[name]
+            ent = roofline_entry(kind, wk, ms, pk, sustained=True)
+            ent.update(ms=round(ms, 5), work=wk, work_unit="bytes" if kind == "hbm" else "flop",
+                       share=round(sum(per[name]) / sum(sum(v) for v in per.values()), 4))
+            kernels[name] = ent
+        dominant = max(KERNELS, key=lambda n: kernels[n]["ms"])
+        top = {k2: kernels[dominant][k2] for k2 in ("bound", "achieved", "peak", "unit", "frac")}
+        top.update(kernel=dominant, traffic=None, peak_kind="sustained bf16 (of measured)"
+                   if top["bound"] == "tensor" else "hbm copy (of measured)", peak_source=pk["source"])
+        value = world * retained * K / (total_ms * 1e-3)
+        result = {
+            "metric": METRIC,
+            "value": value,
+            "unit": UNIT,
+            "n_gpus": world,
+            "steps": K,
+            "warmup": max(3, args.warmup),
+            "ms_per_step": total_ms / K,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16",
+            "data": "synthetic (seeded; Qwen3-30B-A3B-shaped layer, random-init weights)",
+            "config": {
+                "workload": w.name, "T": w.T, "E": w.E, "k": w.k, "h": w.h, "I": w.I,
+                "zipf_s": w.zipf_s, "rho": str(w.rho), "CF": str(w.cf), "retained_pairs": retained,
+                "routed_pairs": w.N, "C": summ["C"], "max_over_mean": round(summ["max_over_mean"], 3),
+                "drop_rate": round(summ["drop_rate"], 5), "parallelism": f"replicas x{world}",
+                "l2": "no flush: inputs larger than L2 (phi 384 MiB, W 384 MiB, g 128 MiB)",
+            },
+            "roofline": top,
+            "kernels": kernels,
+            "gpu_launches": 8 * K,
+            "host_s": round(t_host, 4),
+            "clocks": sampler.summary() if sampler else None,
+        }
+        if not args.no_comparator:
+            result["comparator"] = comparator(rec, d, w, retained, pk)
+        if not args.no_e2e:
+            result["e2e"] = e2e(rec, inp, w, retained, world, min(K, 20))
+        if not args.no_cpu_baseline:
+            result["cpu_baseline"] = cpu_baseline(inp, tokens=args.ref_tokens or 4096, steps=2)
+    rec.close()
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    return result
+
+
+def comparator(rec, d, w, retained, pk, iters=20):
+    """Zero-masked fixed-shape (capacity-padded) GEMMs on the same retained rows."""
+    import torch
+
+    from backward_token_expert_gb300 import lrm as L
+
+    E, C = w.E, rec.C
+    dpad = torch.empty(E * C, w.h, dtype=torch.bfloat16, device="cuda")
+    ppad = torch.empty(E * C, w.I, dtype=torch.bfloat16, device="cuda")
+    poff = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    dphi = torch.empty(E * C, w.I, dtype=torch.bfloat16, device="cuda")
+    dW = torch.empty(E, w.h, w.I, dtype=torch.float32, device="cuda")
+    b = rec.buf
+    s = torch.cuda.current_stream()
+
+    def padded():
+        L.lrm_compact_padded(rec.ctx, b.delta_c, b.phi_c, b.sel_offsets, rec.dims, C, dpad, ppad, poff)
+        L.lrm_grouped_dgrad(rec.ctx, dpad, d["W"], poff, rec.dims, E * C, dphi)
+        L.lrm_grouped_wgrad(rec.ctx, dpad, ppad, poff, rec.dims, E * C, 0, dW)
+
+    def compacted():
+        rec.compact(d["g"], d["phi"], d["alpha"])
+        rec.dgrad(d["W"])
+        rec.wgrad()
+
+    out = {}
+    for name, fn in (("compacted", compacted), ("zero_masked", padded)):
+        for _ in range(3):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(iters):
+            fn()
+        e1.record(s)
+        e1.synchronize()
+        out[name + "_ms"] = round(e0.elapsed_time(e1) / iters, 5)
+    flops_alg = 4 * retained * w.h * w.I
+    flops_pad = 4 * E * C * w.h * w.I
+    out.update(
+        what="compact+dgrad+wgrad on the retained rows vs compact_padded+dgrad+wgrad at M=C per expert",
+        algorithmic_flop=flops_alg, padded_flop=flops_pad, padded_slots=E * C,
+        speedup=round(out["zero_masked_ms"] / out["compacted_ms"], 3),
+        zero_masked_algorithmic_tflops=round(flops_alg / (out["zero_masked_ms"] * 1e-3) / 1e12, 2),
+        compacted_algorithmic_tflops=round(flops_alg / (out["compacted_ms"] * 1e-3) / 1e12, 2))
+    flags = rec.device_status()
+    if flags:
+        raise RuntimeError(f"device status flags {flags:#x} in the comparator")
+    return out
+
+
+def e2e(rec, inp, w, retained, world, iters):
+    """Same metric through the public API with host buffers: pinned host->device
+    copies of the step's inputs, the path, device->host copies of its results."""
+    import torch
+
+    def pinned(a, dtype=None):
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        if dtype is not None:
+            t = t.view(dtype)
+        return t.pin_memory()
+
+    h_in = dict(logits=pinned(inp.logits), expert_idx=pinned(inp.expert_idx), alpha=pinned(inp.alpha),
+                g=pinned(inp.g.view(np.int16), torch.bfloat16), phi=pinned(inp.phi.view(np.int16), torch.bfloat16),
+                W=pinned(inp.W.view(np.int16), torch.bfloat16))
+    dev = {k2: torch.empty_like(v, device="cuda") for k2, v in h_in.items()}
+    b = rec.buf
+    h_out = dict(dW=torch.empty_like(b.dW, device="cpu").pin_memory(),
+                 dphi_c=torch.empty_like(b.dphi_c, device="cpu").pin_memory(),
+                 sel_offsets=torch.empty_like(b.sel_offsets, device="cpu").pin_memory(),
+                 sel_ids=torch.empty_like(b.sel_ids, device="cpu").pin_memory(),
+                 summary=torch.empty_like(b.summary, device="cpu").pin_memory())
+    h2d = sum(v.numel() * v.element_size() for v in h_in.values())
+    d2h = sum(v.numel() * v.element_size() for v in h_out.values())
+
+    def one():
+        for k2, v in h_in.items():
+            dev[k2].copy_(v, non_blocking=True)
+        rec.run(dev["logits"], dev["expert_idx"], dev["g"], dev["phi"], dev["alpha"], dev["W"])
+        h_out["dW"].copy_(b.dW, non_blocking=True)
+        h_out["dphi_c"].copy_(b.dphi_c, non_blocking=True)
+        h_out["sel_offsets"].copy_(b.sel_offsets, non_blocking=True)
+        h_out["sel_ids"].copy_(b.sel_ids, non_blocking=True)
+        h_out["summary"].copy_(b.summary, non_blocking=True)
+
+    for _ in range(2):
+        one()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(iters):
+        one()
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    return {"value": world * retained * iters / dt, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": iters, "ms_per_step": dt * 1e3 / iters,
+            "api": "backward_token_expert_gb300.pipeline.Recalibration.run (C ABI), pinned host buffers"}
+
+
+# ---------------------------------------------------------------------------
+# the fp64 oracle on the host cores (cpu_baseline leg and the reference arm)
+
+
+def token_slice(inp, tokens):
+    import dataclasses
+
+    from workloads.generate import Inputs
+
+    w = inp.workload
+    T = min(tokens, w.T)
+    ws = dataclasses.replace(w, T=T)
+    return Inputs(ws, inp.logits[:T], inp.expert_idx[:T], inp.alpha[: T * w.k], inp.g[:T], inp.phi[: T * w.k],
+                  inp.W, inp.bias)
+
+
+def oracle_step(sl):
+    import oracle as O
+
+    out = O.backward_recalibration(sl)
+    return int(out["stats"]["retained"])
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(inp, tokens, steps):
+    sl = token_slice(inp, tokens)
+    oracle_step(sl)  # warm-up
+    t0 = time.perf_counter()
+    retained = 0
+    for _ in range(steps):
+        retained += oracle_step(sl)
+    dt = time.perf_counter() - t0
+    w = inp.workload
+    return {"value": retained / dt, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"whole path (fp64 numpy oracle) on the first {sl.workload.T} tokens of the "
+                      f"{w.name} layer ({sl.workload.N} routed pairs, same E/k/h/I/CF/rho); "
+                      f"{steps} timed passes after 1 warm-up; BLAS may use all {cpu_cores()} cores, "
+                      "the rest of numpy one",
+            "seconds": round(dt, 3)}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    from workloads import generate, get_workload
+
+    w = get_workload(args.workload)
+    inp = generate(w)
+    K, W = args.steps, max(3, args.warmup)
+    # size the token slice so that K + W passes take about two minutes
+    tokens = args.ref_tokens
+    if not tokens:
+        probe = token_slice(inp, 256)
+        oracle_step(probe)
+        t0 = time.perf_counter()
+        oracle_step(probe)
+        per256 = time.perf_counter() - t0
+        budget = 120.0 / (K + W)
+        tokens = int(max(64, min(w.T, 256 * budget / max(per256, 1e-3))))
+        tokens = max(64, (tokens // 64) * 64)
+    sl = token_slice(inp, tokens)
+    for _ in range(W):
+        oracle_step(sl)
+    t0 = time.perf_counter()
+    retained = 0
+    for _ in range(K):
+        retained += oracle_step(sl)
+    dt = time.perf_counter() - t0
+    value = retained / dt
+    sample = (f"whole path (fp64 numpy oracle) on the first {sl.workload.T} tokens of the {w.name} layer "
+              f"({sl.workload.N} routed pairs per step, same E/k/h/I/CF/rho)")
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": dt * 1e3 / K,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded)",
+        "config": {"workload": w.name, "T": w.T, "E": w.E, "k": w.k, "h": w.h, "I": w.I,
+                   "sample_tokens": sl.workload.T},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+    else:
+        res = run_ours(args, rank, world, local)
+    if rank == 0 and res is not None:
+        print(json.dumps(res))
+
+
+if __name__ == "__main__":
+    main()
