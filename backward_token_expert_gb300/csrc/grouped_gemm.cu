@@ -52,7 +52,8 @@ struct Cfg {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES = (BN == 256) ? 4 : 6;
   static constexpr int TMEM_COLS = 2 * BN;
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
+  static constexpr int STAGING_BYTES = 4 * 32 * 128;  // one [32][32] fp32 store box per epilogue warp
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STAGING_BYTES + 1024;
 };
 
 struct Tile {
@@ -62,7 +63,7 @@ struct Tile {
 template <int MODE, int BN>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        const int32_t* __restrict__ sel_offsets, int E, int h, int I, int max_rows,
+                        const __grid_constant__ CUtensorMap tmOut, const int32_t* __restrict__ sel_offsets, int E, int h, int I, int max_rows,
                         int accumulate, void* __restrict__ out, unsigned int* status,
                         unsigned long long budget_ns) {
   using C = Cfg<BN>;
@@ -285,6 +286,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row_in_tile = q * 32 + lane;
+    uint8_t* stg = smem + C::STAGES * C::STAGE_BYTES + (warp - 2) * (32 * 128);
     uint32_t acc_it = 0;
     for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
       const Tile t = decode(tile);
@@ -333,6 +335,22 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
               }
             }
           }
+        } else if (!accumulate) {
+          // stage the warp's [32 rows][32 cols] fp32 block with the 128-byte
+          // swizzle (16-byte chunk j of row r at chunk j ^ (r % 8)), then one
+          // tensor store; rows past h and columns past I are clipped by TMA
+          if (lane == 0) bulk_wait_read_all();
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<uint4*>(stg + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+                make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(&tmOut, stg, col0, t.mt * BM + q * 32, t.e);
+            bulk_commit_group();
+          }
         } else {
           const int i = t.mt * BM + row_in_tile;
           if (i < h) {
@@ -341,16 +359,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             for (int v = 0; v < 8; ++v) {
               const int col = col0 + v * 4;
               if (col < I) {
-                float4 x = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
-                                       __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
-                if (accumulate) {
-                  const float4 o = *reinterpret_cast<const float4*>(orow + col);
-                  x.x += o.x;
-                  x.y += o.y;
-                  x.z += o.z;
-                  x.w += o.w;
-                }
-                *reinterpret_cast<float4*>(orow + col) = x;
+                const float4 o = *reinterpret_cast<const float4*>(orow + col);
+                *reinterpret_cast<float4*>(orow + col) =
+                    make_float4(o.x + __uint_as_float(r[4 * v]), o.y + __uint_as_float(r[4 * v + 1]),
+                                o.z + __uint_as_float(r[4 * v + 2]), o.w + __uint_as_float(r[4 * v + 3]));
               }
             }
           }
@@ -361,6 +373,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       if (lane == 0) mbar_arrive(&tempty_bar[acc]);
       ++acc_it;
     }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -394,8 +408,21 @@ lrm_status encode_w(lrm_ctx* ctx, CUtensorMap* map, const void* base, uint64_t I
   return r == CUDA_SUCCESS ? LRM_OK : LRM_ERR_CUDA;
 }
 
+// dW [E][h][I] fp32 as a 3-D tensor (I, h, E) with [1][32][32] boxes, 128-byte swizzle.
+lrm_status encode_dw(lrm_ctx* ctx, CUtensorMap* map, const void* base, uint64_t I, uint64_t h, uint64_t E) {
+  const cuuint64_t dims[3] = {I, h, E};
+  const cuuint64_t strides[2] = {I * 4, h * I * 4};
+  const cuuint32_t box[3] = {32, 32, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = ctx->encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides,
+                                 box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                 CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? LRM_OK : LRM_ERR_CUDA;
+}
+
 template <int MODE, int BN>
-lrm_status launch(lrm_ctx* ctx, const CUtensorMap& a, const CUtensorMap& b, const int32_t* sel_offsets,
+lrm_status launch(lrm_ctx* ctx, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
+                  const int32_t* sel_offsets,
                   const lrm_dims& d, int max_rows, int accumulate, void* out, cudaStream_t s) {
   using C = Cfg<BN>;
   auto kern = grouped_gemm_kernel<MODE, BN>;
@@ -405,8 +432,8 @@ lrm_status launch(lrm_ctx* ctx, const CUtensorMap& a, const CUtensorMap& b, cons
     LRM_CHECK_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES));
     configured_device = ctx->device;
   }
-  kern<<<ctx->sm_count, GEMM_THREADS, C::SMEM_BYTES, s>>>(a, b, sel_offsets, d.E, d.h, d.I, max_rows, accumulate,
-                                                          out, ctx->d_status, ctx->wait_budget_ns);
+  kern<<<ctx->sm_count, GEMM_THREADS, C::SMEM_BYTES, s>>>(a, b, o, sel_offsets, d.E, d.h, d.I, max_rows,
+                                                          accumulate, out, ctx->d_status, ctx->wait_budget_ns);
   return launch_status();
 }
 
@@ -439,8 +466,8 @@ extern "C" lrm_status lrm_grouped_dgrad(lrm_ctx* ctx, const uint16_t* delta_c, c
   if ((st = encode_2d(ctx, &ma, delta_c, dims.h, max_rows, BM)) != LRM_OK) return st;
   if ((st = encode_w(ctx, &mb, W, dims.I, dims.h, dims.E)) != LRM_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return use_bn256(dims.I) ? launch<DGRAD, 256>(ctx, ma, mb, sel_offsets, dims, max_rows, 0, dphi_c, s)
-                           : launch<DGRAD, 128>(ctx, ma, mb, sel_offsets, dims, max_rows, 0, dphi_c, s);
+  return use_bn256(dims.I) ? launch<DGRAD, 256>(ctx, ma, mb, ma, sel_offsets, dims, max_rows, 0, dphi_c, s)
+                           : launch<DGRAD, 128>(ctx, ma, mb, ma, sel_offsets, dims, max_rows, 0, dphi_c, s);
 }
 
 extern "C" lrm_status lrm_grouped_wgrad(lrm_ctx* ctx, const uint16_t* delta_c, const uint16_t* phi_c,
@@ -460,10 +487,11 @@ extern "C" lrm_status lrm_grouped_wgrad(lrm_ctx* ctx, const uint16_t* delta_c, c
   const void* a_base = max_rows > 0 ? static_cast<const void*>(delta_c) : static_cast<const void*>(dW);
   const void* b_base = max_rows > 0 ? static_cast<const void*>(phi_c) : static_cast<const void*>(dW);
   const uint64_t rows = max_rows > 0 ? static_cast<uint64_t>(max_rows) : 1;
-  alignas(64) CUtensorMap ma, mb;
+  alignas(64) CUtensorMap ma, mb, mo;
   if ((st = encode_2d(ctx, &ma, a_base, dims.h, rows, 64)) != LRM_OK) return st;
   if ((st = encode_2d(ctx, &mb, b_base, dims.I, rows, 64)) != LRM_OK) return st;
+  if ((st = encode_dw(ctx, &mo, dW, dims.I, dims.h, dims.E)) != LRM_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return use_bn256(dims.I) ? launch<WGRAD, 256>(ctx, ma, mb, sel_offsets, dims, max_rows, accumulate, dW, s)
-                           : launch<WGRAD, 128>(ctx, ma, mb, sel_offsets, dims, max_rows, accumulate, dW, s);
+  return use_bn256(dims.I) ? launch<WGRAD, 256>(ctx, ma, mb, mo, sel_offsets, dims, max_rows, accumulate, dW, s)
+                           : launch<WGRAD, 128>(ctx, ma, mb, mo, sel_offsets, dims, max_rows, accumulate, dW, s);
 }

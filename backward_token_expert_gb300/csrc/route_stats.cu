@@ -6,31 +6,37 @@
 // selection and compaction consume (LRMoE sec. 3.3).
 //
 // Three launches:
-//   rs_count    one block per contiguous chunk of tokens: per-block expert
-//               histogram (shared-memory atomics) and per-block partial sums
-//               of the softmax (one warp per token, fixed reduction order);
+//   rs_count    one block per contiguous chunk of tokens: the chunk's expert
+//               ids are staged in shared memory (validated there), counted
+//               with shared-memory atomics, and the softmax of each token
+//               (one warp per token, the next token's logits prefetched) is
+//               summed per warp in registers, then per block in a fixed order;
 //   rs_finalize one block: counts, offsets, per-(expert, block) bucket bases,
-//               P, f, quotas and the summary;
+//               P, f, quotas and the summary (one warp per expert row of the
+//               expert-major workspace, loads issued eight at a time);
 //   rs_scatter  same chunking as rs_count: stable scatter of pair ids into
 //               the bucket (each warp owns a contiguous sub-range, ranks
 //               inside a warp come from __match_any_sync).
 #include <limits.h>
 #include <math.h>
 
+#include "block_scan.cuh"
 #include "lrm_internal.cuh"
 
 namespace lrm {
 
 namespace {
 
-constexpr int RS_THREADS = 256;
+constexpr int RS_THREADS = 512;
 constexpr int RS_WARPS = RS_THREADS / 32;
 constexpr int RS_PAIRS_PER_BLOCK = 1024;
+constexpr int RS_MAX_PER_THREAD = (RS_PAIRS_PER_BLOCK + RS_THREADS - 1) / RS_THREADS;
 constexpr int RS_FIN_THREADS = 1024;
+constexpr int FIN_UNROLL = 8;
 
 struct RsLayout {
-  int tpb;    // tokens per block
-  int nblk;   // blocks of rs_count / rs_scatter
+  int tpb;   // tokens per block
+  int nblk;  // blocks of rs_count / rs_scatter
   size_t hist_off, p_off, bytes;
 };
 
@@ -46,105 +52,98 @@ RsLayout rs_layout(const lrm_dims& d) {
   return L;
 }
 
-// A pair is valid when its expert id is in range and differs from the ids
-// of the earlier slots of the same token.
-__device__ __forceinline__ bool pair_valid(const int32_t* __restrict__ idx, int p, int k, int E, int e) {
-  if (e < 0 || e >= E) return false;
-  const int t0 = p - (p % k);
-  for (int q = t0; q < p; ++q)
-    if (__ldg(idx + q) == e) return false;
-  return true;
+// Stages the block's pair ids [p0, p1) in shared memory (p0 is the first
+// pair of a token) and replaces every invalid id (outside [0,E) or equal to
+// an earlier slot of the same token) by -1.  Returns true if one was found.
+__device__ __forceinline__ bool stage_ids(const int32_t* __restrict__ idx, int p0, int p1, int k, int E,
+                                          int* s_ids) {
+  for (int p = p0 + static_cast<int>(threadIdx.x); p < p1; p += RS_THREADS) s_ids[p - p0] = __ldg(idx + p);
+  __syncthreads();
+  int fix[RS_MAX_PER_THREAD];
+  int nf = 0;
+  for (int i = threadIdx.x; i < p1 - p0; i += RS_THREADS) {
+    const int e = s_ids[i];
+    bool ok = e >= 0 && e < E;
+    for (int q = i - (i % k); ok && q < i; ++q) ok = s_ids[q] != e;
+    if (!ok) fix[nf++] = i;
+  }
+  __syncthreads();
+  for (int j = 0; j < nf; ++j) s_ids[fix[j]] = -1;
+  __syncthreads();
+  return nf > 0;
 }
 
+template <int VPL>
+__device__ __forceinline__ void load_logits(const float* __restrict__ row, int E, int lane, float (&v)[VPL]) {
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = (e < E) ? __ldg(row + e) : -INFINITY;
+  }
+}
+
+template <int VPL>
 __global__ void __launch_bounds__(RS_THREADS) rs_count(const float* __restrict__ logits,
                                                        const int32_t* __restrict__ idx, int T, int E, int k,
                                                        int tpb, int nblk, int32_t* __restrict__ ws_hist,
                                                        float* __restrict__ ws_p, unsigned int* status) {
   extern __shared__ float rs_smem[];
-  float* pw = rs_smem;                                            // [RS_WARPS][E]
-  int* hist = reinterpret_cast<int*>(rs_smem + RS_WARPS * E);     // [E]
+  float* pw = rs_smem;                                         // [RS_WARPS][E]
+  int* hist = reinterpret_cast<int*>(rs_smem + RS_WARPS * E);  // [E]
+  int* s_ids = hist + E;                                       // [RS_PAIRS_PER_BLOCK]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  for (int i = tid; i < RS_WARPS * E; i += RS_THREADS) pw[i] = 0.f;
   for (int i = tid; i < E; i += RS_THREADS) hist[i] = 0;
-  __syncthreads();
 
   const int tok0 = blockIdx.x * tpb;
   const int tok1 = min(T, tok0 + tpb);
-  bool bad = false;
-  for (int p = tok0 * k + tid; p < tok1 * k; p += RS_THREADS) {
-    const int e = __ldg(idx + p);
-    if (pair_valid(idx, p, k, E, e))
-      atomicAdd(&hist[e], 1);
-    else
-      bad = true;
+  if (stage_ids(idx, tok0 * k, tok1 * k, k, E, s_ids)) raise_flag(status, LRM_ERR_INDEX);
+  for (int i = tid; i < (tok1 - tok0) * k; i += RS_THREADS) {
+    const int e = s_ids[i];
+    if (e >= 0) atomicAdd(&hist[e], 1);
   }
-  if (bad) raise_flag(status, LRM_ERR_INDEX);
 
   // softmax over all E experts, one warp per token; lane owns experts lane + 32 i
-  float* mine = pw + warp * E;
-  for (int t = tok0 + warp; t < tok1; t += RS_WARPS) {
-    const float* row = logits + static_cast<size_t>(t) * E;
-    float v[32];
+  float acc[VPL];
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) acc[i] = 0.f;
+  int t = tok0 + warp;
+  float cur[VPL];
+  if (t < tok1) load_logits<VPL>(logits + static_cast<size_t>(t) * E, E, lane, cur);
+  for (; t < tok1; t += RS_WARPS) {
+    float nxt[VPL];
+    const int tn = t + RS_WARPS;
+    if (tn < tok1) load_logits<VPL>(logits + static_cast<size_t>(tn) * E, E, lane, nxt);
     float mx = -INFINITY;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int e = lane + 32 * i;
-      v[i] = (e < E) ? __ldg(row + e) : -INFINITY;
-      mx = fmaxf(mx, v[i]);
-    }
+    for (int i = 0; i < VPL; ++i) mx = fmaxf(mx, cur[i]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     float s = 0.f;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int e = lane + 32 * i;
-      v[i] = (e < E) ? expf(v[i] - mx) : 0.f;
-      s += v[i];
+    for (int i = 0; i < VPL; ++i) {
+      cur[i] = (lane + 32 * i < E) ? expf(cur[i] - mx) : 0.f;
+      s += cur[i];
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E) mine[e] += v[i] / s;
-    }
+    for (int i = 0; i < VPL; ++i) acc[i] += cur[i] / s;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) cur[i] = nxt[i];
+  }
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E) pw[warp * E + e] = acc[i];
   }
   __syncthreads();
   for (int e = tid; e < E; e += RS_THREADS) {
-    float acc = 0.f;
+    float a = 0.f;
 #pragma unroll
-    for (int w = 0; w < RS_WARPS; ++w) acc += pw[w * E + e];
-    ws_p[static_cast<size_t>(e) * nblk + blockIdx.x] = acc;
+    for (int w = 0; w < RS_WARPS; ++w) a += pw[w * E + e];
+    ws_p[static_cast<size_t>(e) * nblk + blockIdx.x] = a;
     ws_hist[static_cast<size_t>(e) * nblk + blockIdx.x] = hist[e];
   }
-}
-
-// Block-wide exclusive scan of one int per thread (blockDim = 1024).
-__device__ int block_exclusive_scan_1024(int v, int* s_warp, int* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) s_warp[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    int w = s_warp[lane];
-    int z = w;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, z, o);
-      if (lane >= o) z += y;
-    }
-    s_warp[lane] = z - w;
-    if (lane == 31) *total = z;
-  }
-  __syncthreads();
-  const int r = s_warp[warp] + x - v;
-  __syncthreads();
-  return r;
 }
 
 __global__ void __launch_bounds__(RS_FIN_THREADS) rs_finalize(
@@ -169,9 +168,20 @@ __global__ void __launch_bounds__(RS_FIN_THREADS) rs_finalize(
     const size_t row = static_cast<size_t>(x) * nblk;
     int c = 0;
     double ps = 0.0;
-    for (int b = lane; b < nblk; b += 32) {
-      c += ws_hist[row + b];
-      ps += static_cast<double>(ws_p[row + b]);
+    for (int b0 = 0; b0 < nblk; b0 += 32 * FIN_UNROLL) {
+      int hv[FIN_UNROLL];
+      float pv[FIN_UNROLL];
+#pragma unroll
+      for (int j = 0; j < FIN_UNROLL; ++j) {
+        const int b = b0 + lane + 32 * j;
+        hv[j] = b < nblk ? ws_hist[row + b] : 0;
+        pv[j] = b < nblk ? ws_p[row + b] : 0.f;
+      }
+#pragma unroll
+      for (int j = 0; j < FIN_UNROLL; ++j) {
+        c += hv[j];
+        ps += static_cast<double>(pv[j]);
+      }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -197,17 +207,25 @@ __global__ void __launch_bounds__(RS_FIN_THREADS) rs_finalize(
   for (int x = warp; x < E; x += RS_FIN_THREADS / 32) {
     const size_t row = static_cast<size_t>(x) * nblk;
     int run = s_off[x];
-    for (int c0 = 0; c0 < nblk; c0 += 32) {
-      const int b = c0 + lane;
-      const int v = b < nblk ? ws_hist[row + b] : 0;
-      int incl = v;
+    for (int b0 = 0; b0 < nblk; b0 += 32 * FIN_UNROLL) {
+      int hv[FIN_UNROLL];
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
+      for (int j = 0; j < FIN_UNROLL; ++j) {
+        const int b = b0 + lane + 32 * j;
+        hv[j] = b < nblk ? ws_hist[row + b] : 0;
       }
-      if (b < nblk) ws_hist[row + b] = run + incl - v;
-      run += __shfl_sync(0xffffffffu, incl, 31);
+#pragma unroll
+      for (int j = 0; j < FIN_UNROLL; ++j) {
+        const int b = b0 + lane + 32 * j;
+        int incl = hv[j];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        if (b < nblk) ws_hist[row + b] = run + incl - hv[j];
+        run += __shfl_sync(0xffffffffu, incl, 31);
+      }
     }
   }
 
@@ -227,7 +245,7 @@ __global__ void __launch_bounds__(RS_FIN_THREADS) rs_finalize(
   const double fe = (live && N > 0) ? static_cast<double>(cnt) / static_cast<double>(N) : 0.0;
 
   // deterministic block reductions
-  long long vi[6] = {drop, q, live ? cnt : LLONG_MIN, live ? cnt : LLONG_MAX, (live && cnt > 0) ? 1 : 0, 0};
+  long long vi[5] = {drop, q, live ? cnt : LLONG_MIN, live ? cnt : LLONG_MAX, (live && cnt > 0) ? 1 : 0};
   double vd[2] = {fe * Pe, Pe};
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -286,12 +304,13 @@ __global__ void __launch_bounds__(RS_FIN_THREADS) rs_finalize(
 __global__ void __launch_bounds__(RS_THREADS) rs_scatter(const int32_t* __restrict__ idx, int T, int E, int k,
                                                          int tpb, int nblk, const int32_t* __restrict__ ws_base,
                                                          int32_t* __restrict__ bucket) {
-  extern __shared__ int rs_cnt[];  // [RS_WARPS][E]
+  extern __shared__ int rs_cnt[];  // [RS_WARPS][E], then the staged ids
+  int* s_ids = rs_cnt + RS_WARPS * E;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   for (int i = tid; i < RS_WARPS * E; i += RS_THREADS) rs_cnt[i] = 0;
-  __syncthreads();
   const int p0 = blockIdx.x * tpb * k;
   const int p1 = min(T, (blockIdx.x + 1) * tpb) * k;
+  stage_ids(idx, p0, p1, k, E, s_ids);
   const int span = (p1 - p0 + RS_WARPS - 1) / RS_WARPS;
   const int w0 = min(p1, p0 + warp * span);
   const int w1 = min(p1, w0 + span);
@@ -301,11 +320,7 @@ __global__ void __launch_bounds__(RS_THREADS) rs_scatter(const int32_t* __restri
   // pass A: per-warp histogram of its contiguous sub-range
   for (int base = w0; base < w1; base += 32) {
     const int p = base + lane;
-    int e = -1;
-    if (p < w1) {
-      const int v = __ldg(idx + p);
-      if (pair_valid(idx, p, k, E, v)) e = v;
-    }
+    const int e = p < w1 ? s_ids[p - p0] : -1;
     const unsigned peers = __match_any_sync(0xffffffffu, e);
     if (e >= 0 && (peers & lt_mask) == 0) mine[e] += __popc(peers);
     __syncwarp();
@@ -325,11 +340,7 @@ __global__ void __launch_bounds__(RS_THREADS) rs_scatter(const int32_t* __restri
   // pass B: stable placement, ascending pair index within every expert
   for (int base = w0; base < w1; base += 32) {
     const int p = base + lane;
-    int e = -1;
-    if (p < w1) {
-      const int v = __ldg(idx + p);
-      if (pair_valid(idx, p, k, E, v)) e = v;
-    }
+    const int e = p < w1 ? s_ids[p - p0] : -1;
     const unsigned peers = __match_any_sync(0xffffffffu, e);
     int pos = 0;
     if (e >= 0) pos = mine[e] + __popc(peers & lt_mask);
@@ -340,6 +351,18 @@ __global__ void __launch_bounds__(RS_THREADS) rs_scatter(const int32_t* __restri
     }
     __syncwarp();
   }
+}
+
+template <int VPL>
+cudaError_t launch_count(int nblk, size_t smem, cudaStream_t s, const float* logits, const int32_t* idx,
+                         const lrm_dims& d, int tpb, int32_t* ws_hist, float* ws_p, unsigned int* status) {
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(rs_count<VPL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  rs_count<VPL><<<nblk, RS_THREADS, smem, s>>>(logits, idx, d.T, d.E, d.k, tpb, nblk, ws_hist, ws_p, status);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -377,16 +400,32 @@ extern "C" lrm_status lrm_route_stats(lrm_ctx* ctx, const float* logits, const i
   int32_t* ws_hist = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + L.hist_off);
   float* ws_p = reinterpret_cast<float*>(static_cast<char*>(ws) + L.p_off);
   if (L.nblk > 0) {
-    const size_t smem1 = (RS_WARPS + 1) * dims.E * sizeof(float);
-    rs_count<<<L.nblk, RS_THREADS, smem1, s>>>(logits, expert_idx, dims.T, dims.E, dims.k, L.tpb, L.nblk,
-                                               ws_hist, ws_p, ctx->d_status);
-    if ((st = launch_status()) != LRM_OK) return st;
+    const size_t smem1 = (RS_WARPS * dims.E + dims.E + RS_PAIRS_PER_BLOCK) * sizeof(float);
+    const int vpl = (dims.E + 31) / 32;
+    cudaError_t e;
+    if (vpl <= 1)
+      e = launch_count<1>(L.nblk, smem1, s, logits, expert_idx, dims, L.tpb, ws_hist, ws_p, ctx->d_status);
+    else if (vpl <= 2)
+      e = launch_count<2>(L.nblk, smem1, s, logits, expert_idx, dims, L.tpb, ws_hist, ws_p, ctx->d_status);
+    else if (vpl <= 4)
+      e = launch_count<4>(L.nblk, smem1, s, logits, expert_idx, dims, L.tpb, ws_hist, ws_p, ctx->d_status);
+    else if (vpl <= 8)
+      e = launch_count<8>(L.nblk, smem1, s, logits, expert_idx, dims, L.tpb, ws_hist, ws_p, ctx->d_status);
+    else if (vpl <= 16)
+      e = launch_count<16>(L.nblk, smem1, s, logits, expert_idx, dims, L.tpb, ws_hist, ws_p, ctx->d_status);
+    else
+      e = launch_count<32>(L.nblk, smem1, s, logits, expert_idx, dims, L.tpb, ws_hist, ws_p, ctx->d_status);
+    if (e != cudaSuccess) return LRM_ERR_CUDA;
   }
   rs_finalize<<<1, RS_FIN_THREADS, 0, s>>>(dims.T, dims.E, dims.k, L.nblk, cf_num, cf_den, rho_num, rho_den,
                                            ws_hist, ws_p, counts, offsets, P, f, quota, summary);
   if ((st = launch_status()) != LRM_OK) return st;
   if (L.nblk > 0) {
-    const size_t smem3 = RS_WARPS * dims.E * sizeof(int);
+    const size_t smem3 = (RS_WARPS * dims.E + RS_PAIRS_PER_BLOCK) * sizeof(int);
+    if (smem3 > 48 * 1024 &&
+        cudaFuncSetAttribute(rs_scatter, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem3)) !=
+            cudaSuccess)
+      return LRM_ERR_CUDA;
     rs_scatter<<<L.nblk, RS_THREADS, smem3, s>>>(expert_idx, dims.T, dims.E, dims.k, L.tpb, L.nblk, ws_hist,
                                                  bucket);
     if ((st = launch_status()) != LRM_OK) return st;

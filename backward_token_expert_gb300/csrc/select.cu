@@ -4,16 +4,19 @@
 // change which of the equal boundary scores are kept).
 //
 // One 1024-thread block per expert.  Scores are non-negative fp32, so their
-// bit patterns order like the values; a most-significant-digit radix select
-// (four 8-bit digits, warp-aggregated shared-memory histograms) finds the
-// boundary key tau and how many keys equal to tau are still needed.  As soon
-// as a whole histogram bin is taken the search stops and the rule becomes
-// "key >= prefix".  A final pass walks the expert's bucket in ascending pair
-// index and keeps every key above tau plus the first needed keys equal to tau
-// (ties go to the lower pair index), writing them in ascending u with
-// ballot-based block scans.  Keys of experts with at most SEL_SMEM_KEYS
-// candidates stay in shared memory; larger experts re-gather from the score
-// array (which is L2-resident at these sizes) on every pass.
+// bit patterns order like the values.  The block first gathers its
+// candidates' keys (four independent bucket reads and score gathers per
+// thread in flight) into shared memory, or, for an expert with more than
+// SEL_SMEM_KEYS candidates, into its contiguous slice of a workspace.  A
+// most-significant-digit radix select (four 8-bit digits, warp-aggregated
+// shared-memory histograms) then finds the boundary key tau and how many
+// keys equal to tau are still needed; as soon as a whole histogram bin is
+// taken the search stops and the rule becomes "key >= prefix".  The output
+// pass walks the candidates in ascending pair index, eight consecutive per
+// thread, keeps every key above tau plus the first needed keys equal to tau
+// (ties go to the lower pair index), and places them with one packed block
+// scan per 8192 candidates, so the retained ids come out in ascending u.
+#include "block_scan.cuh"
 #include "lrm_internal.cuh"
 
 namespace lrm {
@@ -22,17 +25,20 @@ namespace {
 constexpr int SEL_THREADS = 1024;
 constexpr int SEL_WARPS = SEL_THREADS / 32;
 constexpr int SEL_SMEM_KEYS = 40960;
+constexpr int SEL_GATHER = 4;  // independent gathers in flight per thread
+constexpr int SEL_ITEMS = 8;   // consecutive candidates per thread in the output pass
 
 __device__ __forceinline__ uint32_t score_key(float r) { return __float_as_uint(r) & 0x7FFFFFFFu; }
 
 __global__ void __launch_bounds__(SEL_THREADS, 1)
     select_kernel(const float* __restrict__ R, const int32_t* __restrict__ offsets,
                   const int32_t* __restrict__ bucket, const int32_t* __restrict__ quota, int E, int max_rows,
-                  int32_t* __restrict__ sel_offsets, int32_t* __restrict__ sel_ids, unsigned int* status) {
+                  int32_t* __restrict__ sel_offsets, int32_t* __restrict__ sel_ids, uint32_t* __restrict__ keys_ws,
+                  unsigned int* status) {
   extern __shared__ uint32_t s_keys[];
   __shared__ int s_hist[256];
   __shared__ int s_warp[SEL_WARPS];
-  __shared__ int s_wgt[SEL_WARPS], s_weq[SEL_WARPS];
+  __shared__ int s_total;
   __shared__ int s_digit, s_above, s_bincnt;
 
   const int e = blockIdx.x;
@@ -53,7 +59,8 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
 #pragma unroll 8
   for (int w = 0; w < SEL_WARPS; ++w) base += s_warp[w];
 
-  const int n = max(0, __ldg(offsets + e + 1) - __ldg(offsets + e));
+  const int off = __ldg(offsets + e);
+  const int n = max(0, __ldg(offsets + e + 1) - off);
   const int q_raw = __ldg(quota + e);
   const int q = min(max(q_raw, 0), n);
   if (tid == 0) {
@@ -67,19 +74,31 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
     q_out = max(0, max_rows - base);
   }
   if (q == 0 || q_out == 0) return;
-  const int32_t* src = bucket + __ldg(offsets + e);
+  const int32_t* src = bucket + off;
   int32_t* out = sel_ids + base;
   if (q == n) {
     for (int i = tid; i < q_out; i += SEL_THREADS) out[i] = __ldg(src + i);
     return;
   }
 
-  const bool in_smem = n <= SEL_SMEM_KEYS;
-  if (in_smem) {
-    for (int i = tid; i < n; i += SEL_THREADS) s_keys[i] = score_key(__ldg(R + __ldg(src + i)));
-    __syncthreads();
+  uint32_t* K = (n <= SEL_SMEM_KEYS) ? s_keys : keys_ws + off;
+  for (int i0 = 0; i0 < n; i0 += SEL_THREADS * SEL_GATHER) {
+    int id[SEL_GATHER];
+    float r[SEL_GATHER];
+#pragma unroll
+    for (int j = 0; j < SEL_GATHER; ++j) {
+      const int i = i0 + j * SEL_THREADS + tid;
+      id[j] = i < n ? __ldg(src + i) : -1;
+    }
+#pragma unroll
+    for (int j = 0; j < SEL_GATHER; ++j) r[j] = id[j] >= 0 ? __ldg(R + id[j]) : 0.f;
+#pragma unroll
+    for (int j = 0; j < SEL_GATHER; ++j) {
+      const int i = i0 + j * SEL_THREADS + tid;
+      if (i < n) K[i] = score_key(r[j]);
+    }
   }
-  auto key_at = [&](int i) -> uint32_t { return in_smem ? s_keys[i] : score_key(__ldg(R + __ldg(src + i))); };
+  __syncthreads();
 
   uint32_t prefix = 0, mask = 0;
   int want = q;
@@ -87,15 +106,21 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
   for (int shift = 24; shift >= 0; shift -= 8) {
     if (tid < 256) s_hist[tid] = 0;
     __syncthreads();
-    for (int i0 = 0; i0 < n; i0 += SEL_THREADS) {
-      const int i = i0 + tid;
-      int bin = 256;
-      if (i < n) {
-        const uint32_t kk = key_at(i);
-        if ((kk & mask) == prefix) bin = static_cast<int>((kk >> shift) & 0xFFu);
+    for (int i0 = 0; i0 < n; i0 += SEL_THREADS * SEL_GATHER) {
+      uint32_t kk[SEL_GATHER];
+#pragma unroll
+      for (int j = 0; j < SEL_GATHER; ++j) {
+        const int i = i0 + j * SEL_THREADS + tid;
+        kk[j] = i < n ? K[i] : 0u;
       }
-      const unsigned peers = __match_any_sync(0xffffffffu, bin);
-      if (bin < 256 && (peers & lt_mask) == 0) atomicAdd(&s_hist[bin], __popc(peers));
+#pragma unroll
+      for (int j = 0; j < SEL_GATHER; ++j) {
+        const int i = i0 + j * SEL_THREADS + tid;
+        int bin = 256;
+        if (i < n && (kk[j] & mask) == prefix) bin = static_cast<int>((kk[j] >> shift) & 0xFFu);
+        const unsigned peers = __match_any_sync(0xffffffffu, bin);
+        if (bin < 256 && (peers & lt_mask) == 0) atomicAdd(&s_hist[bin], __popc(peers));
+      }
     }
     __syncthreads();
     // counts of the bins above each bin, from the top bin down
@@ -129,42 +154,52 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
   const uint32_t tau = prefix;
 
   int run_out = 0, run_eq = 0;
-  for (int i0 = 0; i0 < n; i0 += SEL_THREADS) {
-    const int i = i0 + tid;
-    const uint32_t kk = i < n ? key_at(i) : 0u;
-    const bool gt = i < n && (ge_mode ? (kk >= tau) : (kk > tau));
-    const bool eq = i < n && !ge_mode && kk == tau;
-    const unsigned bg = __ballot_sync(0xffffffffu, gt);
-    const unsigned be = __ballot_sync(0xffffffffu, eq);
-    if (lane == 0) {
-      s_wgt[warp] = __popc(bg);
-      s_weq[warp] = __popc(be);
+  for (int i0 = 0; i0 < n; i0 += SEL_THREADS * SEL_ITEMS) {
+    const int ib = i0 + tid * SEL_ITEMS;
+    uint32_t kk[SEL_ITEMS];
+    int id[SEL_ITEMS];
+#pragma unroll
+    for (int j = 0; j < SEL_ITEMS; ++j) {
+      const int i = ib + j;
+      kk[j] = i < n ? K[i] : 0u;
+      id[j] = i < n ? __ldg(src + i) : -1;
     }
-    __syncthreads();
-    int gt_before = __popc(bg & lt_mask), eq_before = __popc(be & lt_mask);
-    int tot_gt = 0, tot_eq = 0;
-    for (int w = 0; w < SEL_WARPS; ++w) {
-      const int a = s_wgt[w], b = s_weq[w];
-      if (w < warp) {
-        gt_before += a;
-        eq_before += b;
-      }
-      tot_gt += a;
-      tot_eq += b;
+    int cg = 0, ce = 0;
+    unsigned gt_bits = 0, eq_bits = 0;
+#pragma unroll
+    for (int j = 0; j < SEL_ITEMS; ++j) {
+      const bool live = ib + j < n;
+      const bool gt = live && (ge_mode ? (kk[j] >= tau) : (kk[j] > tau));
+      const bool eq = live && !ge_mode && kk[j] == tau;
+      gt_bits |= static_cast<unsigned>(gt) << j;
+      eq_bits |= static_cast<unsigned>(eq) << j;
+      cg += gt;
+      ce += eq;
     }
+    const int excl = block_exclusive_scan_1024(cg | (ce << 16), s_warp, &s_total);
+    const int tot = s_total;
     const int eq_left = max(0, want - run_eq);
-    const bool sel = gt || (eq && eq_before < eq_left);
-    const int pos = run_out + gt_before + min(eq_before, eq_left);
-    if (sel && pos < q_out) out[pos] = __ldg(src + i);
-    run_out += tot_gt + min(tot_eq, eq_left);
-    run_eq += tot_eq;
-    __syncthreads();
+    int gtb = excl & 0xFFFF, eqb = excl >> 16;
+#pragma unroll
+    for (int j = 0; j < SEL_ITEMS; ++j) {
+      const bool gt = (gt_bits >> j) & 1u, eq = (eq_bits >> j) & 1u;
+      const bool sel = gt || (eq && eqb < eq_left);
+      const int pos = run_out + gtb + min(eqb, eq_left);
+      if (sel && pos < q_out) out[pos] = id[j];
+      gtb += gt;
+      eqb += eq;
+    }
+    run_out += (tot & 0xFFFF) + min(tot >> 16, eq_left);
+    run_eq += tot >> 16;
   }
 }
 
 }  // namespace
 
-size_t select_workspace_bytes(const lrm_dims&) { return 0; }
+size_t select_workspace_bytes(const lrm_dims& d) {
+  const size_t N = static_cast<size_t>(d.T) * d.k;
+  return N > static_cast<size_t>(SEL_SMEM_KEYS) ? N * sizeof(uint32_t) : 0;
+}
 
 }  // namespace lrm
 
@@ -173,8 +208,6 @@ using namespace lrm;
 extern "C" lrm_status lrm_select(lrm_ctx* ctx, const float* score, const int32_t* offsets, const int32_t* bucket,
                                  const int32_t* quota, lrm_dims dims, int32_t max_rows, int32_t* sel_offsets,
                                  int32_t* sel_ids, void* ws, size_t ws_bytes, void* stream) {
-  (void)ws;
-  (void)ws_bytes;
   if (ctx == nullptr) return LRM_ERR_INVALID_ARG;
   lrm_status st = check_dims(dims);
   if (st != LRM_OK) return st;
@@ -182,7 +215,9 @@ extern "C" lrm_status lrm_select(lrm_ctx* ctx, const float* score, const int32_t
   if (offsets == nullptr || quota == nullptr || sel_offsets == nullptr) return LRM_ERR_INVALID_ARG;
   if (dims.T > 0 && (score == nullptr || bucket == nullptr)) return LRM_ERR_INVALID_ARG;
   if (max_rows > 0 && sel_ids == nullptr) return LRM_ERR_INVALID_ARG;
-  const void* ptrs[] = {score, offsets, bucket, quota, sel_offsets, sel_ids};
+  const size_t need = select_workspace_bytes(dims);
+  if (need > 0 && (ws == nullptr || ws_bytes < need)) return LRM_ERR_WORKSPACE;
+  const void* ptrs[] = {score, offsets, bucket, quota, sel_offsets, sel_ids, ws};
   for (const void* p : ptrs)
     if (p != nullptr && !aligned(p, 4)) return LRM_ERR_ALIGN;
   DeviceGuard guard(ctx->device);
@@ -195,6 +230,7 @@ extern "C" lrm_status lrm_select(lrm_ctx* ctx, const float* score, const int32_t
     configured_device = ctx->device;
   }
   select_kernel<<<dims.E, SEL_THREADS, smem, static_cast<cudaStream_t>(stream)>>>(
-      score, offsets, bucket, quota, dims.E, max_rows, sel_offsets, sel_ids, ctx->d_status);
+      score, offsets, bucket, quota, dims.E, max_rows, sel_offsets, sel_ids, static_cast<uint32_t*>(ws),
+      ctx->d_status);
   return launch_status();
 }

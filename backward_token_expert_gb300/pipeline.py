@@ -51,6 +51,7 @@ class Buffers:
     quota: torch.Tensor
     summary: torch.Tensor
     ws_route: torch.Tensor
+    ws_select: torch.Tensor
     score: torch.Tensor
     sel_offsets: torch.Tensor
     sel_ids: torch.Tensor
@@ -76,6 +77,7 @@ class Recalibration:
         self.max_rows = max_retained_rows(T, E, k, self.cf, self.rho) if max_rows is None else int(max_rows)
         dev = self.device
         ws_bytes = L.lrm_workspace_size(self.ctx, L.LRM_OP_ROUTE_STATS, self.dims)
+        ws_sel = L.lrm_workspace_size(self.ctx, L.LRM_OP_SELECT, self.dims)
         i32 = dict(dtype=torch.int32, device=dev)
         f32 = dict(dtype=torch.float32, device=dev)
         bf = dict(dtype=torch.bfloat16, device=dev)
@@ -89,6 +91,7 @@ class Recalibration:
             quota=torch.empty(E, **i32),
             summary=torch.zeros(L.SUMMARY_BYTES, dtype=torch.uint8, device=dev),
             ws_route=torch.empty(max(256, ws_bytes), dtype=torch.uint8, device=dev),
+            ws_select=torch.empty(max(256, ws_sel), dtype=torch.uint8, device=dev),
             score=torch.empty(max(1, self.N), **f32),
             sel_offsets=torch.empty(E + 1, **i32),
             sel_ids=torch.empty(R, **i32),
@@ -126,7 +129,7 @@ class Recalibration:
     def select(self, stream=None, score=None):
         b = self.buf
         L.lrm_select(self.ctx, b.score if score is None else score, b.offsets, b.bucket, b.quota, self.dims,
-                     self.max_rows, b.sel_offsets, b.sel_ids, None, 0, stream)
+                     self.max_rows, b.sel_offsets, b.sel_ids, b.ws_select, b.ws_select.numel(), stream)
 
     def compact(self, g, phi, alpha, stream=None):
         b = self.buf
