@@ -20,6 +20,8 @@
 #include <limits.h>
 #include <math.h>
 
+#include <mutex>
+
 #include "block_scan.cuh"
 #include "lrm_internal.cuh"
 
@@ -396,6 +398,101 @@ extern "C" lrm_status lrm_route_stats(lrm_ctx* ctx, const float* logits, const i
   if (!aligned(ws, 256)) return LRM_ERR_ALIGN;
   DeviceGuard guard(ctx->device);
   if (!guard.ok) return LRM_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t* ws_hist = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + L.hist_off);
+  float* ws_p = reinterpret_cast<float*>(static_cast<char*>(ws) + L.p_off);
+  if (L.nblk > 0) {
+    const size_t smem1 = (RS_WARPS * dims.E + dims.E + RS_PAIRS_PER_BLOCK) * sizeof(float);
+    const int vpl = (dims.E + 31) / 32;
+    cudaError_t e;
+    if (vpl <= 1)
+      e = launch_count<1>(L.nblk, smem1, s, logits, expert_idx, dims, L.tpb, ws_hist, ws_p, ctx->d_status);
+    else if (vpl <= 2)
+      e = launch_count<2>(L.nblk, smem1, s, logits, expert_idx, dims, L.tpb, ws_hist, ws_p, ctx->d_status);
+    else if (vpl <= 4)
+      e = launch_count<4>(L.nblk, smem1, s, logits, expert_idx, dims, L.tpb, ws_hist, ws_p, ctx->d_status);
+    else if (vpl <= 8)
+      e = launch_count<8>(L.nblk, smem1, s, logits, expert_idx, dims, L.tpb, ws_hist, ws_p, ctx->d_status);
+    else if (vpl <= 16)
+      e = launch_count<16>(L.nblk, smem1, s, logits, expert_idx, dims, L.tpb, ws_hist, ws_p, ctx->d_status);
+    else
+      e = launch_count<32>(L.nblk, smem1, s, logits, expert_idx, dims, L.tpb, ws_hist, ws_p, ctx->d_status);
+    if (e != cudaSuccess) return LRM_ERR_CUDA;
+  }
+  rs_finalize<<<1, RS_FIN_THREADS, 0, s>>>(dims.T, dims.E, dims.k, L.nblk, cf_num, cf_den, rho_num, rho_den,
+                                           ws_hist, ws_p, counts, offsets, P, f, quota, summary);
+  if ((st = launch_status()) != LRM_OK) return st;
+  if (L.nblk > 0) {
+    const size_t smem3 = (RS_WARPS * dims.E + RS_PAIRS_PER_BLOCK) * sizeof(int);
+    if (smem3 > 48 * 1024 &&
+        cudaFuncSetAttribute(rs_scatter, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem3)) !=
+            cudaSuccess)
+      return LRM_ERR_CUDA;
+    rs_scatter<<<L.nblk, RS_THREADS, smem3, s>>>(expert_idx, dims.T, dims.E, dims.k, L.tpb, L.nblk, ws_hist,
+                                                 bucket);
+    if ((st = launch_status()) != LRM_OK) return st;
+  }
+  return LRM_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Variant without a caller workspace, for callers that cannot allocate device
+// memory: the scratch of the three kernels is this fixed array.  Host code
+// only sees a stand-in symbol for it, so its device address is looked up
+// once per device (with that device current) and passed to the kernels.
+
+namespace lrm {
+namespace {
+
+static __device__ __align__(256) unsigned char g_route_stats_scratch[LRM_ROUTE_STATS_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mutex;
+void* g_scratch_addr[kMaxDevices] = {};
+
+// Device address of g_route_stats_scratch on the current device (cached).
+lrm_status scratch_address(int device, void** out) {
+  if (device < 0 || device >= kMaxDevices) return LRM_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (g_scratch_addr[device] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_route_stats_scratch) != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      return LRM_ERR_CUDA;
+    }
+    g_scratch_addr[device] = p;
+  }
+  *out = g_scratch_addr[device];
+  return LRM_OK;
+}
+
+}  // namespace
+}  // namespace lrm
+
+extern "C" lrm_status lrm_route_stats_noalloc(lrm_ctx* ctx, const float* logits, const int32_t* expert_idx,
+                                              lrm_dims dims, int32_t cf_num, int32_t cf_den, int32_t rho_num,
+                                              int32_t rho_den, int32_t* counts, int32_t* offsets, int32_t* bucket,
+                                              float* P, float* f, int32_t* quota, lrm_route_summary* summary,
+                                              void* stream) {
+  if (ctx == nullptr) return LRM_ERR_INVALID_ARG;
+  lrm_status st = check_dims(dims);
+  if (st != LRM_OK) return st;
+  if (cf_num <= 0 || cf_den <= 0 || rho_den <= 0 || rho_num < 0 || rho_num > rho_den)
+    return LRM_ERR_INVALID_ARG;
+  if (counts == nullptr || offsets == nullptr || P == nullptr || f == nullptr || quota == nullptr ||
+      summary == nullptr)
+    return LRM_ERR_INVALID_ARG;
+  if (dims.T > 0 && (logits == nullptr || expert_idx == nullptr || bucket == nullptr))
+    return LRM_ERR_INVALID_ARG;
+  const void* ptrs[] = {logits, expert_idx, counts, offsets, bucket, P, f, quota, summary};
+  for (const void* p : ptrs)
+    if (p != nullptr && !aligned(p, 4)) return LRM_ERR_ALIGN;
+  const RsLayout L = rs_layout(dims);
+  if (L.bytes > LRM_ROUTE_STATS_SCRATCH_BYTES) return LRM_ERR_SHAPE;
+  DeviceGuard guard(ctx->device);
+  if (!guard.ok) return LRM_ERR_CUDA;
+  void* ws = nullptr;
+  if ((st = scratch_address(ctx->device, &ws)) != LRM_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int32_t* ws_hist = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + L.hist_off);
   float* ws_p = reinterpret_cast<float*>(static_cast<char*>(ws) + L.p_off);

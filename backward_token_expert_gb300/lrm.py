@@ -52,7 +52,11 @@ EXPORTED = (
     "lrm_get_device_status",
     "lrm_set_wait_budget",
     "lrm_selftest_wait_timeout",
+    "lrm_route_stats_noalloc",
 )
+
+# bytes of the library's fixed scratch array used by lrm_route_stats_noalloc
+ROUTE_STATS_SCRATCH_BYTES = 4 << 20
 
 
 class LrmError(RuntimeError):
@@ -119,6 +123,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "lrm_get_device_status": ([P, P, ctypes.POINTER(ctypes.c_uint32)], st),
         "lrm_set_wait_budget": ([P, ctypes.c_uint64], st),
         "lrm_selftest_wait_timeout": ([P, ctypes.c_uint64, P], st),
+        "lrm_route_stats_noalloc": ([P, P, P, Dims, i32, i32, i32, i32, P, P, P, P, P, P, P, P], st),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -199,6 +204,18 @@ def lrm_route_stats(ctx, logits, expert_idx, dims: Dims, cf, rho, counts, offset
                                           _ptr(offsets), _ptr(bucket), _ptr(P), _ptr(f), _ptr(quota),
                                           _ptr(summary), _ptr(ws), int(ws_bytes), _stream(stream)),
            "lrm_route_stats")
+
+
+def lrm_route_stats_noalloc(ctx, logits, expert_idx, dims: Dims, cf, rho, counts, offsets, bucket, P, f, quota,
+                            summary, stream=None) -> None:
+    """lrm_route_stats with the library's fixed scratch array instead of a workspace."""
+    cf = Fraction(cf)
+    rho = Fraction(rho)
+    _check(load_library().lrm_route_stats_noalloc(ctx, _ptr(logits), _ptr(expert_idx), dims, cf.numerator,
+                                                  cf.denominator, rho.numerator, rho.denominator, _ptr(counts),
+                                                  _ptr(offsets), _ptr(bucket), _ptr(P), _ptr(f), _ptr(quota),
+                                                  _ptr(summary), _stream(stream)),
+           "lrm_route_stats_noalloc")
 
 
 def lrm_score(ctx, g, phi, alpha, dims: Dims, score, stream=None) -> None:

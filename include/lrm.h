@@ -224,6 +224,40 @@ LRM_API lrm_status lrm_compact_padded(lrm_ctx* ctx, const uint16_t* delta_c, con
                               const int32_t* sel_offsets, lrm_dims dims, int32_t C, uint16_t* delta_pad,
                               uint16_t* phi_pad, int32_t* pad_offsets, void* stream);
 
+/*
+ * lrm_route_stats without a caller-provided workspace: the same three kernels
+ * and the same outputs, but the scratch they need lives in a fixed array
+ * inside this library (LRM_ROUTE_STATS_SCRATCH_BYTES of device memory, held
+ * on every GPU that loads the library until the process exits).
+ *
+ * It is meant for callers that hold only the tensors they pass in and cannot
+ * obtain extra device memory: for example a host framework whose memory pool
+ * owns the GPU's memory and forbids outside allocation, or code that must not
+ * allocate once it is running.  The call itself allocates nothing: no
+ * cudaMalloc, cudaFree or allocating library routine.
+ *
+ * - The scratch holds two E x B tables of 4-byte entries, one column per
+ *   block of floor(1024 / k) tokens (B = ceil(T / floor(1024 / k)), about
+ *   8 * E * T * k / 1024 bytes); sizes that do not fit in
+ *   LRM_ROUTE_STATS_SCRATCH_BYTES (4 MiB: for example E = 128 with up to
+ *   about 4 million routed pairs) return LRM_ERR_SHAPE before any device
+ *   work.  Every entry is written before it is read, so nothing in the
+ *   scratch has to start at zero and stale contents of an earlier call are
+ *   harmless.
+ * - The first call on a device looks up the array's device address (with
+ *   that device current) and caches it; make that first call before any
+ *   stream capture.
+ * - All calls share the one array, so calls that may overlap on the GPU
+ *   (different streams without ordering between them) race; serialise them.
+ * The paper has no counterpart of this entry point.
+ */
+#define LRM_ROUTE_STATS_SCRATCH_BYTES (4u << 20)
+LRM_API lrm_status lrm_route_stats_noalloc(lrm_ctx* ctx, const float* logits, const int32_t* expert_idx,
+                                           lrm_dims dims, int32_t cf_num, int32_t cf_den, int32_t rho_num,
+                                           int32_t rho_den, int32_t* counts, int32_t* offsets, int32_t* bucket,
+                                           float* P, float* f, int32_t* quota, lrm_route_summary* summary,
+                                           void* stream);
+
 /* Synchronise `stream`, return the device status word in *flags (bit
  * (1u << code) for every lrm_status code raised on the device since the last
  * read) and clear it. */
