@@ -383,6 +383,402 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   if (warp == 1) tmem_dealloc(tmem_base, C::TMEM_COLS);
 }
 
+// ---------------------------------------------------------------------------
+// wgrad on CTA pairs: dW_e [h, I] in 256 x BN output tiles, one per cluster of
+// two CTAs.  CTA r of a pair loads rows [128r, 128r + 128) of the tile's M
+// (= h) range of delta_c^T and columns [r BN/2, (r+1) BN/2) of phi_c into its
+// own 6-stage ring (32 KiB per stage); the even CTA issues the M = 256
+// tcgen05.mma.cta_group::2, which reads both CTAs' shared memory, so each B
+// byte crosses L2 once per pair.  Each CTA's TMEM holds its 128 rows x BN.
+//   warp 0   TMA producer of the CTA's halves.  Full K blocks: both CTAs'
+//            loads count their bytes on the even CTA's full barrier
+//            (cta_group::2 TMA) and the even CTA gives the phase's two
+//            arrivals.  The ragged last K block of an expert: each CTA loads
+//            into its own "tail" barrier instead.
+//   warp 1   even CTA: waits for the stage, issues the pair MMAs and
+//            multicasts the commits to both CTAs' empty / accumulator-full
+//            barriers (idle in the odd CTA)
+//   warps 2-9 epilogue of the CTA's own 128 rows, two warps per TMEM lane
+//            quarter (each takes half of the BN columns; TMEM chunks are
+//            prefetched one ahead), TMA tensor stores, then release the
+//            accumulator on the even CTA's barrier (16 arrivals)
+//   warp 10  tail fixer: waits for the CTA's own tail load, zeroes the rows
+//            of its halves that lie past the expert's segment (the MMA reads
+//            whole 16-row K steps) and arrives on the even CTA's full barrier
+//            (release at cluster scope), off the MMA warp's path
+
+template <int BN>
+struct CfgPair {
+  static constexpr int A_BYTES = 128 * BK * 2;       // this CTA's 128 rows of M
+  static constexpr int B_BYTES = (BN / 2) * BK * 2;  // this CTA's BN/2 columns of N
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = 5;
+  static constexpr int TMEM_COLS = 2 * BN;
+  static constexpr int EPI_WARPS = 8;                       // two per TMEM lane quarter
+  static constexpr int THREADS = 64 + 32 * EPI_WARPS + 32;  // + the tail fixer warp
+  static constexpr int FIXER_WARP = 2 + EPI_WARPS;
+  static constexpr int STAGING_BYTES = EPI_WARPS * 32 * 128;  // one [32][32] fp32 store box per epilogue warp
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STAGING_BYTES + 1024;
+};
+
+// Start row and length of expert e's segment, clamped to the buffers.
+__device__ __forceinline__ void segment(const int32_t* __restrict__ sel_offsets, int e, int max_rows, int& start,
+                                        int& len) {
+  int st = __ldg(sel_offsets + e), en = __ldg(sel_offsets + e + 1);
+  st = min(max(st, 0), max_rows);
+  en = min(max(en, st), max_rows);
+  start = st;
+  len = en - st;
+}
+
+template <int BN>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CfgPair<BN>::THREADS, 1)
+    wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                      const __grid_constant__ CUtensorMap tmOut, const int32_t* __restrict__ sel_offsets, int E,
+                      int h, int I, int max_rows, int accumulate, float* __restrict__ out, unsigned int* status,
+                      unsigned long long budget_ns) {
+  using C = CfgPair<BN>;
+  extern __shared__ uint8_t dsmem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsmem_raw) + 1023) & ~uintptr_t(1023));
+
+  __shared__ __align__(8) uint64_t full_bar[C::STAGES];
+  __shared__ __align__(8) uint64_t tail_bar[C::STAGES];
+  __shared__ __align__(8) uint64_t empty_bar[C::STAGES];
+  __shared__ __align__(8) uint64_t tfull_bar[2];
+  __shared__ __align__(8) uint64_t tempty_bar[2];
+  __shared__ __align__(8) uint64_t drain_bar;
+  __shared__ uint32_t s_tmem_base;
+  __shared__ int s_abort;
+  __shared__ int s_len[MAX_E];
+  __shared__ uint16_t s_order[MAX_E];  // experts by descending retained rows (ties: lower id)
+  static_assert(C::STAGES <= 32, "tail parities are kept in one 32-bit mask");
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+  const int tiles_n = (I + BN - 1) / BN;
+  const int tiles_m = (h + 255) / 256;
+  const int per_expert = tiles_m * tiles_n;
+  const int total_tiles = E * per_expert;
+
+  // Schedule: the pair tiles of all experts, heaviest expert first, dealt to
+  // the pairs in a snake order (round r goes forward for even r, backward for
+  // odd r), which balances the ragged K loops across pairs.
+  for (int e = tid; e < E; e += C::THREADS) {
+    int st, ln;
+    segment(sel_offsets, e, max_rows, st, ln);
+    s_len[e] = ln;
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += C::THREADS) {
+    const int le = s_len[e];
+    int rank = 0;
+    for (int x = 0; x < E; ++x) {
+      const int lx = s_len[x];
+      rank += (lx > le) || (lx == le && x < e);
+    }
+    s_order[rank] = static_cast<uint16_t>(e);
+  }
+  if (tid == 0) {
+    s_abort = 0;
+    if (blockIdx.x == 0 && __ldg(sel_offsets + E) > max_rows) raise_flag(status, LRM_ERR_SHAPE);
+    for (int i = 0; i < C::STAGES; ++i) {
+      mbar_init(&full_bar[i], 2);  // full block: the even CTA twice; tail block: each fixer once
+      mbar_init(&tail_bar[i], 1);
+      mbar_init(&empty_bar[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull_bar[i], 1);
+      mbar_init(&tempty_bar[i], 2 * C::EPI_WARPS);
+    }
+    mbar_init(&drain_bar, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(&s_tmem_base, C::TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // both CTAs' barriers exist before any cross-CTA signal
+  tc_fence_after();
+  const uint32_t tmem_base = s_tmem_base;
+  volatile int* abort_flag = &s_abort;
+  auto fail = [&]() {
+    *abort_flag = 1;
+    raise_flag(status, LRM_ERR_TIMEOUT);
+  };
+  auto tile_of = [&](int round) { return round * npairs + ((round & 1) ? npairs - 1 - pair : pair); };
+  auto decode = [&](int tile, int& e, int& mt, int& nt) {
+    const int slot = tile / per_expert;
+    e = s_order[slot];
+    const int rem = tile - slot * per_expert;
+    mt = rem / tiles_n;
+    nt = rem - mt * tiles_n;
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmB);
+      const uint32_t full0 = mapa_shared(&full_bar[0], 0);  // the even CTA's full barriers
+      uint32_t it = 0, tail_par = 0;
+      bool ok = true;
+      for (int round = 0, tile = tile_of(0); tile < total_tiles && ok; tile = tile_of(++round)) {
+        int e, mt, nt;
+        decode(tile, e, mt, nt);
+        int start, len;
+        segment(sel_offsets, e, max_rows, start, len);
+        const int nkb = (len + BK - 1) / BK;
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const uint32_t s = it % C::STAGES;
+          const uint32_t ph = (it / C::STAGES) & 1u;
+          if (!mbar_wait(&empty_bar[s], ph ^ 1u, budget_ns, abort_flag)) {
+            fail();
+            ok = false;
+            break;
+          }
+          uint8_t* a_dst = smem + s * C::STAGE_BYTES;
+          uint8_t* b_dst = a_dst + C::A_BYTES;
+          const int xa = mt * 256 + static_cast<int>(rank) * 128;
+          const int xb = nt * BN + static_cast<int>(rank) * (BN / 2);
+          const int y = start + kb * BK;
+          if (len - kb * BK >= BK) {
+            if (leader) {
+              // both arrivals of a full block come from here; the odd CTA's
+              // loads only add their bytes
+              mbar_arrive_expect_tx(&full_bar[s], 2 * C::STAGE_BYTES);
+              mbar_arrive(&full_bar[s]);
+            }
+            const uint32_t bar = full0 + s * 8;
+#pragma unroll
+            for (int c = 0; c < 2; ++c) tma_load_2d_pair(a_dst + c * ATOM_BYTES, &tmA, bar, xa + c * 64, y);
+#pragma unroll
+            for (int c = 0; c < BN / 128; ++c) tma_load_2d_pair(b_dst + c * ATOM_BYTES, &tmB, bar, xb + c * 64, y);
+          } else {
+            mbar_arrive_expect_tx(&tail_bar[s], C::STAGE_BYTES);
+#pragma unroll
+            for (int c = 0; c < 2; ++c) tma_load_2d(a_dst + c * ATOM_BYTES, &tmA, &tail_bar[s], xa + c * 64, y);
+#pragma unroll
+            for (int c = 0; c < BN / 128; ++c)
+              tma_load_2d(b_dst + c * ATOM_BYTES, &tmB, &tail_bar[s], xb + c * 64, y);
+            tail_par ^= 1u << s;
+          }
+        }
+      }
+      // the even CTA's commits arrive on these barriers asynchronously: wait
+      // for the release of the last STAGES stages so none is still in flight
+      // when the block exits (also lets issued copies land after a timeout)
+      for (uint32_t j = it; j < it + C::STAGES; ++j)
+        if (!mbar_wait(&empty_bar[j % C::STAGES], ((j / C::STAGES) & 1u) ^ 1u, budget_ns, ok ? abort_flag : nullptr))
+          break;
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (even CTA)
+    constexpr uint32_t idesc = idesc_bf16_f32(256, BN, 1u, 1u);
+    uint32_t it = 0, acc_it = 0;
+    bool ok = leader;
+    for (int round = 0, tile = tile_of(0); tile < total_tiles && ok; tile = tile_of(++round)) {
+      int e, mt, nt;
+      decode(tile, e, mt, nt);
+      int start, len;
+      segment(sel_offsets, e, max_rows, start, len);
+      const int nkb = (len + BK - 1) / BK;
+      if (nkb == 0) continue;
+      const uint32_t acc = acc_it & 1u;
+      const uint32_t aph = (acc_it >> 1) & 1u;
+      if (!__all_sync(0xffffffffu, mbar_wait_cluster(&tempty_bar[acc], aph ^ 1u, budget_ns, abort_flag))) {
+        if (lane == 0) fail();
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + acc * BN;
+      for (int kb = 0; kb < nkb; ++kb, ++it) {
+        const uint32_t s = it % C::STAGES;
+        const uint32_t ph = (it / C::STAGES) & 1u;
+        const int valid = len - kb * BK;
+        const bool tail = valid < BK;
+        const int nk = tail ? (valid + 15) / 16 : BK / 16;
+        // a tail stage was zero-filled by the fixer warps of both CTAs
+        const bool got = tail ? mbar_wait_cluster(&full_bar[s], ph, budget_ns, abort_flag)
+                              : mbar_wait(&full_bar[s], ph, budget_ns, abort_flag);
+        if (!__all_sync(0xffffffffu, got)) {
+          if (lane == 0) fail();
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t a_addr = smem_u32(smem + s * C::STAGE_BYTES);
+          const uint32_t b_addr = a_addr + C::A_BYTES;
+          for (int kk = 0; kk < nk; ++kk) {
+            const uint64_t adesc = smem_desc_sw128(a_addr + kk * 2048, ATOM_BYTES, 1024);
+            const uint64_t bdesc = smem_desc_sw128(b_addr + kk * 2048, ATOM_BYTES, 1024);
+            mma_bf16_ss_pair(d_tmem, adesc, bdesc, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit_pair_multicast(&empty_bar[s]);
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
+      if (lane == 0) mma_commit_pair_multicast(&tfull_bar[acc]);
+      __syncwarp();
+      ++acc_it;
+    }
+    if (leader) {
+      if (lane == 0) {
+        mma_commit_pair_local(&drain_bar);
+        if (!mbar_wait(&drain_bar, 0, budget_ns, nullptr)) raise_flag(status, LRM_ERR_TIMEOUT);
+      }
+      __syncwarp();
+    }
+  } else if (warp == C::FIXER_WARP) {
+    // ------------------------------------------------------------ tail fixer
+    const uint32_t full0 = mapa_shared(&full_bar[0], 0);
+    uint32_t it = 0, tail_par = 0;
+    bool ok = true;
+    for (int round = 0, tile = tile_of(0); tile < total_tiles && ok; tile = tile_of(++round)) {
+      int e, mt, nt;
+      decode(tile, e, mt, nt);
+      int start, len;
+      segment(sel_offsets, e, max_rows, start, len);
+      const int nkb = (len + BK - 1) / BK;
+      if (nkb == 0) continue;
+      it += nkb - 1;  // full blocks need no fixing
+      const int valid = len - (nkb - 1) * BK;
+      if (valid < BK) {
+        const uint32_t s = it % C::STAGES;
+        const uint32_t tph = (tail_par >> s) & 1u;
+        tail_par ^= 1u << s;
+        if (!__all_sync(0xffffffffu, mbar_wait(&tail_bar[s], tph, budget_ns, abort_flag))) {
+          if (lane == 0) fail();
+          ok = false;
+          break;
+        }
+        uint8_t* a_stage = smem + s * C::STAGE_BYTES;
+        uint8_t* b_stage = a_stage + C::A_BYTES;
+        // rows [valid, 16 ceil(valid/16)) of this CTA's halves lie past the segment
+        const int nz = ((valid + 15) / 16) * 16 - valid;
+        constexpr int atoms = 2 + BN / 128;
+        const int units = nz * 8 * atoms;
+        for (int i = lane; i < units; i += 32) {
+          const int atom = i / (nz * 8);
+          const int rem = i - atom * nz * 8;
+          uint8_t* base = atom < 2 ? a_stage + atom * ATOM_BYTES : b_stage + (atom - 2) * ATOM_BYTES;
+          *reinterpret_cast<uint4*>(base + (valid + rem / 8) * 128 + (rem % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          if (leader)
+            mbar_arrive(&full_bar[s]);
+          else
+            mbar_arrive_cluster(full0 + s * 8);
+        }
+        __syncwarp();
+      }
+      ++it;
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;                  // TMEM lane quarter this warp may access
+    const int c_begin = ((warp - 2) >> 2) * (BN / 2);  // this warp's half of the columns
+    const int row_in_half = q * 32 + lane;
+    uint8_t* stg = smem + C::STAGES * C::STAGE_BYTES + (warp - 2) * (32 * 128);
+    const uint32_t tempty0 = mapa_shared(&tempty_bar[0], 0);
+    uint32_t acc_it = 0;
+    for (int round = 0, tile = tile_of(0); tile < total_tiles; tile = tile_of(++round)) {
+      int e, mt, nt;
+      decode(tile, e, mt, nt);
+      const int row0 = mt * 256 + static_cast<int>(rank) * 128;  // first dW row of this CTA's half
+      int start, len;
+      segment(sel_offsets, e, max_rows, start, len);
+      if (len == 0) {
+        if (!accumulate) {
+          const int i = row0 + row_in_half;
+          if (i < h) {
+            float* orow = out + (static_cast<size_t>(e) * h + i) * I;
+            for (int c = c_begin; c < c_begin + BN / 2; c += 4) {
+              const int col = nt * BN + c;
+              if (col < I) *reinterpret_cast<float4*>(orow + col) = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+          }
+        }
+        continue;
+      }
+      const uint32_t acc = acc_it & 1u;
+      const uint32_t aph = (acc_it >> 1) & 1u;
+      if (!__all_sync(0xffffffffu, mbar_wait(&tfull_bar[acc], aph, budget_ns, abort_flag))) {
+        if (lane == 0) fail();
+        break;
+      }
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN + c_begin;
+      uint32_t r[32], nx[32];
+      tmem_ld_32x32b_x32(taddr, r);
+      tmem_ld_wait();
+      for (int c = 0; c < BN / 2; c += 32) {
+        const bool more = c + 32 < BN / 2;
+        if (more) tmem_ld_32x32b_x32(taddr + c + 32, nx);  // next chunk in flight while this one is stored
+        const int col0 = nt * BN + c_begin + c;
+        if (!accumulate) {
+          if (lane == 0) bulk_wait_read_all();
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<uint4*>(stg + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+                make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(&tmOut, stg, col0, row0 + q * 32, e);
+            bulk_commit_group();
+          }
+        } else {
+          const int i = row0 + row_in_half;
+          if (i < h) {
+            float* orow = out + (static_cast<size_t>(e) * h + i) * I;
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+              const int col = col0 + v * 4;
+              if (col < I) {
+                const float4 o = *reinterpret_cast<const float4*>(orow + col);
+                *reinterpret_cast<float4*>(orow + col) =
+                    make_float4(o.x + __uint_as_float(r[4 * v]), o.y + __uint_as_float(r[4 * v + 1]),
+                                o.z + __uint_as_float(r[4 * v + 2]), o.w + __uint_as_float(r[4 * v + 3]));
+              }
+            }
+          }
+        }
+        if (more) {
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) r[j] = nx[j];
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (leader)
+          mbar_arrive(&tempty_bar[acc]);
+        else
+          mbar_arrive_cluster(tempty0 + acc * 8);
+      }
+      ++acc_it;
+    }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // no CTA leaves while its partner may still read its shared memory or TMEM
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+}
+
 // Row-major 2-D bf16 tensor [rows][cols] with [box_rows][64] boxes.
 lrm_status encode_2d(lrm_ctx* ctx, CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
                      uint32_t box_rows) {
@@ -434,6 +830,32 @@ lrm_status launch(lrm_ctx* ctx, const CUtensorMap& a, const CUtensorMap& b, cons
   }
   kern<<<ctx->sm_count, GEMM_THREADS, C::SMEM_BYTES, s>>>(a, b, o, sel_offsets, d.E, d.h, d.I, max_rows,
                                                           accumulate, out, ctx->d_status, ctx->wait_budget_ns);
+  return launch_status();
+}
+
+template <int BN>
+lrm_status launch_wgrad_pair(lrm_ctx* ctx, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
+                             const int32_t* sel_offsets, const lrm_dims& d, int max_rows, int accumulate, float* out,
+                             cudaStream_t s) {
+  using C = CfgPair<BN>;
+  auto kern = wgrad_pair_kernel<BN>;
+  static thread_local int configured_device = -1;
+  static thread_local int clusters = 0;
+  if (configured_device != ctx->device) {
+    if (ctx->smem_optin < C::SMEM_BYTES + 1024) return LRM_ERR_ARCH;
+    LRM_CHECK_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(ctx->sm_count & ~1, 1, 1);
+    cfg.blockDim = dim3(C::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    int n = 0;
+    LRM_CHECK_CUDA(cudaOccupancyMaxActiveClusters(&n, kern, &cfg));
+    if (n < 1) return LRM_ERR_ARCH;
+    clusters = n;
+    configured_device = ctx->device;
+  }
+  kern<<<2 * clusters, C::THREADS, C::SMEM_BYTES, s>>>(a, b, o, sel_offsets, d.E, d.h, d.I, max_rows, accumulate,
+                                                         out, ctx->d_status, ctx->wait_budget_ns);
   return launch_status();
 }
 
@@ -492,6 +914,5 @@ extern "C" lrm_status lrm_grouped_wgrad(lrm_ctx* ctx, const uint16_t* delta_c, c
   if ((st = encode_2d(ctx, &mb, b_base, dims.I, rows, 64)) != LRM_OK) return st;
   if ((st = encode_dw(ctx, &mo, dW, dims.I, dims.h, dims.E)) != LRM_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return use_bn256(dims.I) ? launch<WGRAD, 256>(ctx, ma, mb, mo, sel_offsets, dims, max_rows, accumulate, dW, s)
-                           : launch<WGRAD, 128>(ctx, ma, mb, mo, sel_offsets, dims, max_rows, accumulate, dW, s);
+  return launch_wgrad_pair<256>(ctx, ma, mb, mo, sel_offsets, dims, max_rows, accumulate, dW, s);
 }

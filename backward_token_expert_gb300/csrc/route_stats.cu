@@ -157,9 +157,9 @@ __global__ void __launch_bounds__(RS_FIN_THREADS) rs_finalize(
   __shared__ int s_total;
   __shared__ int s_cnt[1024];
   __shared__ int s_off[1024];
-  __shared__ double s_P[1024];
+  __shared__ float s_P[1024];
   __shared__ long long s_red_i[6][32];
-  __shared__ double s_red_d[2][32];
+  __shared__ float s_red_d[2][32];
   const int e = threadIdx.x;
   const int lane = e & 31, warp = e >> 5;
   const bool live = e < E;
@@ -169,7 +169,7 @@ __global__ void __launch_bounds__(RS_FIN_THREADS) rs_finalize(
   for (int x = warp; x < E; x += RS_FIN_THREADS / 32) {
     const size_t row = static_cast<size_t>(x) * nblk;
     int c = 0;
-    double ps = 0.0;
+    float ps = 0.f;
     for (int b0 = 0; b0 < nblk; b0 += 32 * FIN_UNROLL) {
       int hv[FIN_UNROLL];
       float pv[FIN_UNROLL];
@@ -182,7 +182,7 @@ __global__ void __launch_bounds__(RS_FIN_THREADS) rs_finalize(
 #pragma unroll
       for (int j = 0; j < FIN_UNROLL; ++j) {
         c += hv[j];
-        ps += static_cast<double>(pv[j]);
+        ps += pv[j];
       }
     }
 #pragma unroll
@@ -233,22 +233,23 @@ __global__ void __launch_bounds__(RS_FIN_THREADS) rs_finalize(
 
   // capacity and quota in exact integer arithmetic
   const long long C = (static_cast<long long>(cf_num) * N) / (static_cast<long long>(cf_den) * E);
-  double Pe = 0.0;
+  // fp32 throughout: fp64 runs at a small fraction of the fp32 rate on this part
+  float Pe = 0.f;
   long long q = 0, drop = 0;
   if (live) {
-    Pe = (T > 0) ? s_P[e] / T : 0.0;
+    Pe = (T > 0) ? s_P[e] / static_cast<float>(T) : 0.f;
     const long long m = cnt < C ? cnt : C;
     q = (static_cast<long long>(rho_num) * m + rho_den - 1) / rho_den;
     drop = cnt > C ? cnt - C : 0;
-    P[e] = static_cast<float>(Pe);
-    f[e] = N > 0 ? static_cast<float>(static_cast<double>(cnt) / static_cast<double>(N)) : 0.f;
+    P[e] = Pe;
+    f[e] = N > 0 ? static_cast<float>(cnt) / static_cast<float>(N) : 0.f;
     quota[e] = static_cast<int32_t>(q);
   }
-  const double fe = (live && N > 0) ? static_cast<double>(cnt) / static_cast<double>(N) : 0.0;
+  const float fe = (live && N > 0) ? static_cast<float>(cnt) / static_cast<float>(N) : 0.f;
 
   // deterministic block reductions
   long long vi[5] = {drop, q, live ? cnt : LLONG_MIN, live ? cnt : LLONG_MAX, (live && cnt > 0) ? 1 : 0};
-  double vd[2] = {fe * Pe, Pe};
+  float vd[2] = {fe * Pe, Pe};
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     vi[0] += __shfl_xor_sync(0xffffffffu, vi[0], o);
@@ -270,7 +271,7 @@ __global__ void __launch_bounds__(RS_FIN_THREADS) rs_finalize(
     long long a0 = lane < nw ? s_red_i[0][lane] : 0, a1 = lane < nw ? s_red_i[1][lane] : 0;
     long long a2 = lane < nw ? s_red_i[2][lane] : LLONG_MIN, a3 = lane < nw ? s_red_i[3][lane] : LLONG_MAX;
     long long a4 = lane < nw ? s_red_i[4][lane] : 0;
-    double d0 = lane < nw ? s_red_d[0][lane] : 0.0, d1 = lane < nw ? s_red_d[1][lane] : 0.0;
+    float d0 = lane < nw ? s_red_d[0][lane] : 0.f, d1 = lane < nw ? s_red_d[1][lane] : 0.f;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       a0 += __shfl_xor_sync(0xffffffffu, a0, o);
@@ -291,13 +292,12 @@ __global__ void __launch_bounds__(RS_FIN_THREADS) rs_finalize(
       s.max_count = static_cast<int32_t>(a2);
       s.min_count = static_cast<int32_t>(a3);
       s.nonempty = static_cast<int32_t>(a4);
-      s.aux_unscaled = static_cast<float>(E * d0);
-      s.drop_rate = N > 0 ? static_cast<float>(static_cast<double>(a0) / static_cast<double>(N)) : 0.f;
-      s.util = C > 0 ? static_cast<float>(static_cast<double>(N - a0) / static_cast<double>(C * E)) : 0.f;
-      s.rho_real = N > 0 ? static_cast<float>(static_cast<double>(a1) / static_cast<double>(N)) : 0.f;
-      s.max_over_mean =
-          N > 0 ? static_cast<float>(static_cast<double>(a2) * E / static_cast<double>(N)) : 0.f;
-      s.sum_P = static_cast<float>(d1);
+      s.aux_unscaled = static_cast<float>(E) * d0;
+      s.drop_rate = N > 0 ? static_cast<float>(a0) / static_cast<float>(N) : 0.f;
+      s.util = C > 0 ? static_cast<float>(N - a0) / static_cast<float>(C * E) : 0.f;
+      s.rho_real = N > 0 ? static_cast<float>(a1) / static_cast<float>(N) : 0.f;
+      s.max_over_mean = N > 0 ? static_cast<float>(a2) * static_cast<float>(E) / static_cast<float>(N) : 0.f;
+      s.sum_P = d1;
       *summary = s;
     }
   }

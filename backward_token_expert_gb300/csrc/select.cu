@@ -3,19 +3,21 @@
 // keeping the largest scores of every expert is optimal, and ties only
 // change which of the equal boundary scores are kept).
 //
-// One 1024-thread block per expert.  Scores are non-negative fp32, so their
-// bit patterns order like the values.  The block first gathers its
-// candidates' keys (four independent bucket reads and score gathers per
-// thread in flight) into shared memory, or, for an expert with more than
-// SEL_SMEM_KEYS candidates, into its contiguous slice of a workspace.  A
-// most-significant-digit radix select (four 8-bit digits, warp-aggregated
-// shared-memory histograms) then finds the boundary key tau and how many
-// keys equal to tau are still needed; as soon as a whole histogram bin is
-// taken the search stops and the rule becomes "key >= prefix".  The output
-// pass walks the candidates in ascending pair index, eight consecutive per
-// thread, keeps every key above tau plus the first needed keys equal to tau
-// (ties go to the lower pair index), and places them with one packed block
-// scan per 8192 candidates, so the retained ids come out in ascending u.
+// Two launches.  select_gather_kernel reads the scores in bucket order over
+// the whole GPU (four independent bucket reads and score gathers in flight
+// per thread) and writes them as sortable keys into a contiguous
+// expert-major workspace: scores are non-negative fp32, so their bit
+// patterns order like the values.  select_kernel then runs one 1024-thread
+// block per expert on its contiguous key slice (cached in shared memory when
+// it holds at most SEL_SMEM_KEYS keys): a most-significant-digit radix select
+// with 11/11/10-bit digits and warp-aggregated shared-memory histograms finds
+// the boundary key tau and how many keys equal to tau are still needed; as
+// soon as a whole histogram bin is taken the search stops and the rule
+// becomes "key >= prefix".  The output pass walks the candidates in
+// ascending pair index, eight consecutive per thread, keeps every key above
+// tau plus the first needed keys equal to tau (ties go to the lower pair
+// index), and places them with one packed block scan per 8192 candidates, so
+// the retained ids come out in ascending u.
 #include "block_scan.cuh"
 #include "lrm_internal.cuh"
 
@@ -25,18 +27,42 @@ namespace {
 constexpr int SEL_THREADS = 1024;
 constexpr int SEL_WARPS = SEL_THREADS / 32;
 constexpr int SEL_SMEM_KEYS = 40960;
-constexpr int SEL_GATHER = 4;  // independent gathers in flight per thread
+constexpr int SEL_GATHER = 4;  // independent loads in flight per thread
+constexpr int SEL_MAX_BINS = 2048;
+constexpr int GATHER_THREADS = 256;
 constexpr int SEL_ITEMS = 8;   // consecutive candidates per thread in the output pass
 
 __device__ __forceinline__ uint32_t score_key(float r) { return __float_as_uint(r) & 0x7FFFFFFFu; }
 
+__global__ void __launch_bounds__(GATHER_THREADS) select_gather_kernel(const float* __restrict__ R,
+                                                                       const int32_t* __restrict__ bucket, int N,
+                                                                       uint32_t* __restrict__ keys) {
+  const int stride = gridDim.x * GATHER_THREADS * SEL_GATHER;
+  for (int i0 = blockIdx.x * GATHER_THREADS * SEL_GATHER + threadIdx.x; i0 < N; i0 += stride) {
+    int id[SEL_GATHER];
+#pragma unroll
+    for (int j = 0; j < SEL_GATHER; ++j) {
+      const int i = i0 + j * GATHER_THREADS;
+      id[j] = i < N ? __ldg(bucket + i) : -1;
+    }
+    float r[SEL_GATHER];
+#pragma unroll
+    for (int j = 0; j < SEL_GATHER; ++j) r[j] = (id[j] >= 0 && id[j] < N) ? __ldg(R + id[j]) : 0.f;
+#pragma unroll
+    for (int j = 0; j < SEL_GATHER; ++j) {
+      const int i = i0 + j * GATHER_THREADS;
+      if (i < N) keys[i] = score_key(r[j]);
+    }
+  }
+}
+
 __global__ void __launch_bounds__(SEL_THREADS, 1)
     select_kernel(const float* __restrict__ R, const int32_t* __restrict__ offsets,
                   const int32_t* __restrict__ bucket, const int32_t* __restrict__ quota, int E, int max_rows,
-                  int32_t* __restrict__ sel_offsets, int32_t* __restrict__ sel_ids, uint32_t* __restrict__ keys_ws,
-                  unsigned int* status) {
+                  int32_t* __restrict__ sel_offsets, int32_t* __restrict__ sel_ids,
+                  const uint32_t* __restrict__ keys_ws, unsigned int* status) {
   extern __shared__ uint32_t s_keys[];
-  __shared__ int s_hist[256];
+  __shared__ int s_hist[SEL_MAX_BINS];
   __shared__ int s_warp[SEL_WARPS];
   __shared__ int s_total;
   __shared__ int s_digit, s_above, s_bincnt;
@@ -81,30 +107,34 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
     return;
   }
 
-  uint32_t* K = (n <= SEL_SMEM_KEYS) ? s_keys : keys_ws + off;
-  for (int i0 = 0; i0 < n; i0 += SEL_THREADS * SEL_GATHER) {
-    int id[SEL_GATHER];
-    float r[SEL_GATHER];
+  const uint32_t* K = keys_ws + off;
+  if (n <= SEL_SMEM_KEYS) {
+    for (int i0 = 0; i0 < n; i0 += SEL_THREADS * SEL_GATHER) {
+      uint32_t v[SEL_GATHER];
 #pragma unroll
-    for (int j = 0; j < SEL_GATHER; ++j) {
-      const int i = i0 + j * SEL_THREADS + tid;
-      id[j] = i < n ? __ldg(src + i) : -1;
+      for (int j = 0; j < SEL_GATHER; ++j) {
+        const int i = i0 + j * SEL_THREADS + tid;
+        v[j] = i < n ? __ldg(K + i) : 0u;
+      }
+#pragma unroll
+      for (int j = 0; j < SEL_GATHER; ++j) {
+        const int i = i0 + j * SEL_THREADS + tid;
+        if (i < n) s_keys[i] = v[j];
+      }
     }
-#pragma unroll
-    for (int j = 0; j < SEL_GATHER; ++j) r[j] = id[j] >= 0 ? __ldg(R + id[j]) : 0.f;
-#pragma unroll
-    for (int j = 0; j < SEL_GATHER; ++j) {
-      const int i = i0 + j * SEL_THREADS + tid;
-      if (i < n) K[i] = score_key(r[j]);
-    }
+    K = s_keys;
   }
   __syncthreads();
 
   uint32_t prefix = 0, mask = 0;
   int want = q;
   bool ge_mode = false;
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    if (tid < 256) s_hist[tid] = 0;
+  for (int pass = 0; pass < 3; ++pass) {
+    const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+    const int bits = pass == 2 ? 10 : 11;
+    const int nbins = 1 << bits;
+    const uint32_t dmask = static_cast<uint32_t>(nbins - 1);
+    for (int b = tid; b < nbins; b += SEL_THREADS) s_hist[b] = 0;
     __syncthreads();
     for (int i0 = 0; i0 < n; i0 += SEL_THREADS * SEL_GATHER) {
       uint32_t kk[SEL_GATHER];
@@ -116,34 +146,32 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
 #pragma unroll
       for (int j = 0; j < SEL_GATHER; ++j) {
         const int i = i0 + j * SEL_THREADS + tid;
-        int bin = 256;
-        if (i < n && (kk[j] & mask) == prefix) bin = static_cast<int>((kk[j] >> shift) & 0xFFu);
+        int bin = SEL_MAX_BINS;
+        if (i < n && (kk[j] & mask) == prefix) bin = static_cast<int>((kk[j] >> shift) & dmask);
         const unsigned peers = __match_any_sync(0xffffffffu, bin);
-        if (bin < 256 && (peers & lt_mask) == 0) atomicAdd(&s_hist[bin], __popc(peers));
+        if (bin < SEL_MAX_BINS && (peers & lt_mask) == 0) atomicAdd(&s_hist[bin], __popc(peers));
       }
     }
     __syncthreads();
-    // counts of the bins above each bin, from the top bin down
-    const int c = tid < 256 ? s_hist[255 - tid] : 0;
-    int incl = c;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    if (lane == 31) s_warp[warp] = incl;
-    __syncthreads();
-    int above = incl - c;
-    for (int w = 0; w < warp; ++w) above += s_warp[w];
-    if (tid < 256 && above < want && want <= above + c) {
-      s_digit = 255 - tid;
+    // thread t owns bins hi = nbins-1-2t and hi-1 (descending); "above" counts
+    // every key of the current prefix in a higher bin
+    const int hi = nbins - 1 - 2 * tid;
+    const int c_hi = hi >= 0 ? s_hist[hi] : 0;
+    const int c_lo = hi >= 1 ? s_hist[hi - 1] : 0;
+    const int above = block_exclusive_scan_1024(c_hi + c_lo, s_warp, &s_total);
+    if (hi >= 0 && above < want && want <= above + c_hi) {
+      s_digit = hi;
       s_above = above;
-      s_bincnt = c;
+      s_bincnt = c_hi;
+    } else if (hi >= 1 && above + c_hi < want && want <= above + c_hi + c_lo) {
+      s_digit = hi - 1;
+      s_above = above + c_hi;
+      s_bincnt = c_lo;
     }
     __syncthreads();
     want -= s_above;
     prefix |= static_cast<uint32_t>(s_digit) << shift;
-    mask |= 0xFFu << shift;
+    mask |= dmask << shift;
     const bool all_taken = (s_bincnt == want);
     __syncthreads();
     if (all_taken) {
@@ -196,10 +224,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
 
 }  // namespace
 
-size_t select_workspace_bytes(const lrm_dims& d) {
-  const size_t N = static_cast<size_t>(d.T) * d.k;
-  return N > static_cast<size_t>(SEL_SMEM_KEYS) ? N * sizeof(uint32_t) : 0;
-}
+size_t select_workspace_bytes(const lrm_dims& d) { return static_cast<size_t>(d.T) * d.k * sizeof(uint32_t); }
 
 }  // namespace lrm
 
@@ -229,8 +254,17 @@ extern "C" lrm_status lrm_select(lrm_ctx* ctx, const float* score, const int32_t
         cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)));
     configured_device = ctx->device;
   }
-  select_kernel<<<dims.E, SEL_THREADS, smem, static_cast<cudaStream_t>(stream)>>>(
-      score, offsets, bucket, quota, dims.E, max_rows, sel_offsets, sel_ids, static_cast<uint32_t*>(ws),
-      ctx->d_status);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int N = dims.T * dims.k;
+  if (N > 0) {
+    const int per_block = GATHER_THREADS * SEL_GATHER;
+    const int need_blocks = (N + per_block - 1) / per_block;
+    const int cap = ctx->sm_count * 8;
+    select_gather_kernel<<<need_blocks < cap ? need_blocks : cap, GATHER_THREADS, 0, s>>>(
+        score, bucket, N, static_cast<uint32_t*>(ws));
+    if ((st = launch_status()) != LRM_OK) return st;
+  }
+  select_kernel<<<dims.E, SEL_THREADS, smem, s>>>(score, offsets, bucket, quota, dims.E, max_rows, sel_offsets,
+                                                  sel_ids, static_cast<const uint32_t*>(ws), ctx->d_status);
   return launch_status();
 }

@@ -117,14 +117,14 @@ def check_route_stats(gpu, inp, st):
     assert np.array_equal(gpu["offsets"], st["offsets"])
     assert np.array_equal(gpu["bucket"], st["bucket"])
     assert np.all(rel_close(gpu["P"], st["P"], STAT_RTOL, 1e-30))
-    assert np.all(rel_close(gpu["f"], st["f"], 1e-7, 0))
+    assert np.all(rel_close(gpu["f"], st["f"], 2.5e-7, 0))  # two fp32 roundings
     s = gpu["summary"]
     assert s["N"] == st["N"] and s["C"] == st["C"] and s["slots"] == st["slots"]
     assert s["dropped"] == st["dropped"]
     assert s["max_count"] == int(st["counts"].max()) and s["min_count"] == int(st["counts"].min())
     assert s["nonempty"] == int((st["counts"] > 0).sum())
     assert abs(s["aux_unscaled"] - st["aux"]) <= STAT_RTOL * st["aux"]
-    assert abs(s["drop_rate"] - st["drop_rate"]) <= 1e-7
+    assert abs(s["drop_rate"] - st["drop_rate"]) <= 2.5e-7 * max(st["drop_rate"], 1e-30) + 1e-12
     assert abs(s["util"] - st["util"]) <= 1e-6
     assert abs(s["max_over_mean"] - st["max_over_mean"]) <= 1e-6 * st["max_over_mean"]
     assert abs(s["sum_P"] - 1.0) <= 1e-5
