@@ -9,15 +9,21 @@
 // expert-major workspace: scores are non-negative fp32, so their bit
 // patterns order like the values.  select_kernel then runs one 1024-thread
 // block per expert on its contiguous key slice (cached in shared memory when
-// it holds at most SEL_SMEM_KEYS keys): a most-significant-digit radix select
-// with 11/11/10-bit digits and warp-aggregated shared-memory histograms finds
-// the boundary key tau and how many keys equal to tau are still needed; as
-// soon as a whole histogram bin is taken the search stops and the rule
-// becomes "key >= prefix".  The output pass walks the candidates in
-// ascending pair index, eight consecutive per thread, keeps every key above
-// tau plus the first needed keys equal to tau (ties go to the lower pair
-// index), and places them with one packed block scan per 8192 candidates, so
-// the retained ids come out in ascending u.
+// it holds at most SEL_SMEM_KEYS keys):
+//  - experts with more than SEL_SAMPLE_MIN candidates first sort a sample of
+//    1024 keys, bracket the boundary between two sample keys, count the keys
+//    above and inside the bracket with ballots and keep only the bracket's
+//    keys when the boundary lies inside (else they fall back to all keys);
+//  - a most-significant-digit radix select (11/11/10-bit digits,
+//    warp-aggregated shared-memory histograms) finds the boundary key; once
+//    the boundary bin fits in SEL_CAND_KEYS its keys are compacted and later
+//    passes scan only them; as soon as a whole bin is taken the rule becomes
+//    "key >= prefix";
+//  - the output pass gives each warp a contiguous range of candidates in
+//    ascending pair index, counts its kept keys with ballots, scans the 32
+//    warp totals and places every kept id, keeping the first needed keys
+//    equal to the boundary (ties go to the lower pair index), so the
+//    retained ids come out in ascending u.
 #include "block_scan.cuh"
 #include "lrm_internal.cuh"
 
@@ -30,7 +36,9 @@ constexpr int SEL_SMEM_KEYS = 40960;
 constexpr int SEL_GATHER = 4;  // independent loads in flight per thread
 constexpr int SEL_MAX_BINS = 2048;
 constexpr int GATHER_THREADS = 256;
-constexpr int SEL_ITEMS = 8;   // consecutive candidates per thread in the output pass
+constexpr int SEL_CAND_KEYS = 8192;  // shared-memory room for the boundary bin's keys
+constexpr int SEL_OUT_UNROLL = 16;   // 32-candidate steps whose loads are issued together
+constexpr int SEL_SAMPLE_MIN = 4096; // experts with more candidates bracket the boundary by sampling
 
 __device__ __forceinline__ uint32_t score_key(float r) { return __float_as_uint(r) & 0x7FFFFFFFu; }
 
@@ -62,9 +70,11 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
                   int32_t* __restrict__ sel_offsets, int32_t* __restrict__ sel_ids,
                   const uint32_t* __restrict__ keys_ws, unsigned int* status) {
   extern __shared__ uint32_t s_keys[];
+  uint32_t* s_cand = s_keys + SEL_SMEM_KEYS;  // [SEL_CAND_KEYS] keys of the boundary bin
   __shared__ int s_hist[SEL_MAX_BINS];
   __shared__ int s_warp[SEL_WARPS];
-  __shared__ int s_total;
+  __shared__ int s_wgt[SEL_WARPS], s_weq[SEL_WARPS];
+  __shared__ int s_total, s_ncand;
   __shared__ int s_digit, s_above, s_bincnt;
 
   const int e = blockIdx.x;
@@ -127,15 +137,38 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
   __syncthreads();
 
   uint32_t prefix = 0, mask = 0;
-  int want = q;
+  int want = q;           // keys still to take from C
   bool ge_mode = false;
-  for (int pass = 0; pass < 3; ++pass) {
-    const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
-    const int bits = pass == 2 ? 10 : 11;
-    const int nbins = 1 << bits;
-    const uint32_t dmask = static_cast<uint32_t>(nbins - 1);
-    for (int b = tid; b < nbins; b += SEL_THREADS) s_hist[b] = 0;
+  uint32_t ge_floor = 0;  // in "key >= prefix" mode, keys below ge_floor are not candidates
+  const uint32_t* C = K;  // keys the next radix pass scans
+  int nc = n;
+  if (n > SEL_SAMPLE_MIN) {
+    // Sample select: sort 1024 evenly spaced keys (descending, bitonic), take
+    // the sample keys a few standard deviations either side of the expected
+    // rank of the boundary, count the keys above and inside that bracket with
+    // ballots, and if the boundary lies inside, keep only the bracket's keys.
+    uint32_t* samp = reinterpret_cast<uint32_t*>(s_hist);
+    samp[tid] = K[static_cast<int>((static_cast<long long>(tid) * n) / SEL_THREADS)];
     __syncthreads();
+    for (int kk = 2; kk <= SEL_THREADS; kk <<= 1) {
+      for (int j = kk >> 1; j > 0; j >>= 1) {
+        const int ixj = tid ^ j;
+        if (ixj > tid) {
+          const uint32_t a = samp[tid], b = samp[ixj];
+          if (((tid & kk) == 0) ? (a < b) : (a > b)) {
+            samp[tid] = b;
+            samp[ixj] = a;
+          }
+        }
+        __syncthreads();
+      }
+    }
+    const float pr = static_cast<float>(q) / static_cast<float>(n);
+    const int r = min(SEL_THREADS - 1, static_cast<int>((static_cast<long long>(q) * SEL_THREADS) / n));
+    const int d = static_cast<int>(3.f * sqrtf(SEL_THREADS * pr * (1.f - pr))) + 8;
+    const uint32_t hi = samp[max(0, r - d)];
+    const uint32_t lo = samp[min(SEL_THREADS - 1, r + d)];
+    int c_gt = 0, c_in = 0;
     for (int i0 = 0; i0 < n; i0 += SEL_THREADS * SEL_GATHER) {
       uint32_t kk[SEL_GATHER];
 #pragma unroll
@@ -145,80 +178,178 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
       }
 #pragma unroll
       for (int j = 0; j < SEL_GATHER; ++j) {
-        const int i = i0 + j * SEL_THREADS + tid;
-        int bin = SEL_MAX_BINS;
-        if (i < n && (kk[j] & mask) == prefix) bin = static_cast<int>((kk[j] >> shift) & dmask);
-        const unsigned peers = __match_any_sync(0xffffffffu, bin);
-        if (bin < SEL_MAX_BINS && (peers & lt_mask) == 0) atomicAdd(&s_hist[bin], __popc(peers));
+        const bool live = i0 + j * SEL_THREADS + tid < n;
+        c_gt += __popc(__ballot_sync(0xffffffffu, live && kk[j] > hi));
+        c_in += __popc(__ballot_sync(0xffffffffu, live && kk[j] >= lo && kk[j] <= hi));
       }
     }
-    __syncthreads();
-    // thread t owns bins hi = nbins-1-2t and hi-1 (descending); "above" counts
-    // every key of the current prefix in a higher bin
-    const int hi = nbins - 1 - 2 * tid;
-    const int c_hi = hi >= 0 ? s_hist[hi] : 0;
-    const int c_lo = hi >= 1 ? s_hist[hi - 1] : 0;
-    const int above = block_exclusive_scan_1024(c_hi + c_lo, s_warp, &s_total);
-    if (hi >= 0 && above < want && want <= above + c_hi) {
-      s_digit = hi;
-      s_above = above;
-      s_bincnt = c_hi;
-    } else if (hi >= 1 && above + c_hi < want && want <= above + c_hi + c_lo) {
-      s_digit = hi - 1;
-      s_above = above + c_hi;
-      s_bincnt = c_lo;
+    if (lane == 0) {
+      s_wgt[warp] = c_gt;
+      s_weq[warp] = c_in;
     }
     __syncthreads();
-    want -= s_above;
-    prefix |= static_cast<uint32_t>(s_digit) << shift;
-    mask |= dmask << shift;
-    const bool all_taken = (s_bincnt == want);
-    __syncthreads();
-    if (all_taken) {
-      ge_mode = true;
-      break;
+    c_gt = 0;
+    c_in = 0;
+    for (int w = 0; w < SEL_WARPS; ++w) {
+      c_gt += s_wgt[w];
+      c_in += s_weq[w];
+    }
+    if (c_gt < q && q <= c_gt + c_in && c_in <= SEL_CAND_KEYS) {
+      if (tid == 0) s_ncand = 0;
+      __syncthreads();
+      for (int i0 = 0; i0 < n; i0 += SEL_THREADS) {
+        const int i = i0 + tid;
+        const uint32_t kk = i < n ? K[i] : 0u;
+        const bool m = i < n && kk >= lo && kk <= hi;
+        const unsigned bal = __ballot_sync(0xffffffffu, m);
+        int wbase = 0;
+        if (lane == 0 && bal != 0u) wbase = atomicAdd(&s_ncand, __popc(bal));
+        wbase = __shfl_sync(0xffffffffu, wbase, 0);
+        if (m) s_cand[wbase + __popc(bal & lt_mask)] = kk;
+      }
+      __syncthreads();
+      C = s_cand;
+      nc = c_in;
+      want = q - c_gt;
+      ge_floor = lo;
+    }
+    __syncthreads();  // the sample buffer is the histogram below
+  }
+  // radix select of the want-th largest key of C: digits of at most 11 bits
+  // from the top; the first one (bits 21-31) sees the sign-free exponent and
+  // the leading mantissa bits, where keys bunch into few bins and the
+  // warp-aggregated atomics stay cheap
+  {
+    int lo_bit = 32;  // bits [lo_bit, 32) of the boundary key are known
+    while (lo_bit > 0) {
+      const int bits = min(11, lo_bit);
+      const int shift = lo_bit - bits;
+      const int nbins = 1 << bits;
+      const uint32_t dmask = static_cast<uint32_t>(nbins - 1);
+      for (int b = tid; b < nbins; b += SEL_THREADS) s_hist[b] = 0;
+      __syncthreads();
+      for (int i0 = 0; i0 < nc; i0 += SEL_THREADS * SEL_GATHER) {
+        uint32_t kk[SEL_GATHER];
+#pragma unroll
+        for (int j = 0; j < SEL_GATHER; ++j) {
+          const int i = i0 + j * SEL_THREADS + tid;
+          kk[j] = i < nc ? C[i] : 0u;
+        }
+#pragma unroll
+        for (int j = 0; j < SEL_GATHER; ++j) {
+          const int i = i0 + j * SEL_THREADS + tid;
+          int bin = SEL_MAX_BINS;
+          if (i < nc && (kk[j] & mask) == prefix) bin = static_cast<int>((kk[j] >> shift) & dmask);
+          const unsigned peers = __match_any_sync(0xffffffffu, bin);
+          if (bin < SEL_MAX_BINS && (peers & lt_mask) == 0) atomicAdd(&s_hist[bin], __popc(peers));
+        }
+      }
+      __syncthreads();
+      // thread t owns bins hi = nbins-1-2t and hi-1 (descending); "above" counts
+      // every key of the current prefix in a higher bin
+      const int hi = nbins - 1 - 2 * tid;
+      const int c_hi = hi >= 0 ? s_hist[hi] : 0;
+      const int c_lo = hi >= 1 ? s_hist[hi - 1] : 0;
+      const int above = block_exclusive_scan_1024(c_hi + c_lo, s_warp, &s_total);
+      if (hi >= 0 && above < want && want <= above + c_hi) {
+        s_digit = hi;
+        s_above = above;
+        s_bincnt = c_hi;
+      } else if (hi >= 1 && above + c_hi < want && want <= above + c_hi + c_lo) {
+        s_digit = hi - 1;
+        s_above = above + c_hi;
+        s_bincnt = c_lo;
+      }
+      __syncthreads();
+      want -= s_above;
+      prefix |= static_cast<uint32_t>(s_digit) << shift;
+      mask |= dmask << shift;
+      const int bincnt = s_bincnt;
+      __syncthreads();
+      lo_bit = shift;
+      if (bincnt == want) {  // the whole bin is kept: "key >= prefix"
+        ge_mode = true;
+        break;
+      }
+      if (lo_bit == 0) break;
+      // once the boundary bin fits, later passes scan only its keys
+      if (C == K && bincnt <= SEL_CAND_KEYS) {
+        if (tid == 0) s_ncand = 0;
+        __syncthreads();
+        for (int i0 = 0; i0 < nc; i0 += SEL_THREADS) {
+          const int i = i0 + tid;
+          const uint32_t kk = i < nc ? C[i] : 0u;
+          const bool m = i < nc && (kk & mask) == prefix;
+          const unsigned bal = __ballot_sync(0xffffffffu, m);
+          int wbase = 0;
+          if (lane == 0 && bal != 0u) wbase = atomicAdd(&s_ncand, __popc(bal));
+          wbase = __shfl_sync(0xffffffffu, wbase, 0);
+          if (m) s_cand[wbase + __popc(bal & lt_mask)] = kk;
+        }
+        __syncthreads();
+        C = s_cand;
+        nc = s_ncand;
+      }
     }
   }
-  const uint32_t tau = prefix;
+  const uint32_t tau = ge_mode ? max(prefix, ge_floor) : prefix;
 
-  int run_out = 0, run_eq = 0;
-  for (int i0 = 0; i0 < n; i0 += SEL_THREADS * SEL_ITEMS) {
-    const int ib = i0 + tid * SEL_ITEMS;
-    uint32_t kk[SEL_ITEMS];
-    int id[SEL_ITEMS];
+  // Output: each warp owns a contiguous range of the candidates (ascending u).
+  // Count its kept keys, scan the 32 warp totals, then place the kept ids:
+  // key x goes to (#keys above tau before x) + min(#keys equal to tau before
+  // x, want), keeping the first `want` keys equal to tau.
+  const int span = ((n + SEL_WARPS - 1) / SEL_WARPS + 31) & ~31;
+  const int w0 = min(n, warp * span), w1 = min(n, w0 + span);
+  int cg = 0, ce = 0;
+  for (int i0 = w0; i0 < w1; i0 += 32 * SEL_OUT_UNROLL) {
+    uint32_t kk[SEL_OUT_UNROLL];
 #pragma unroll
-    for (int j = 0; j < SEL_ITEMS; ++j) {
-      const int i = ib + j;
-      kk[j] = i < n ? K[i] : 0u;
-      id[j] = i < n ? __ldg(src + i) : -1;
+    for (int j = 0; j < SEL_OUT_UNROLL; ++j) {
+      const int i = i0 + 32 * j + lane;
+      kk[j] = i < w1 ? K[i] : 0u;
     }
-    int cg = 0, ce = 0;
-    unsigned gt_bits = 0, eq_bits = 0;
 #pragma unroll
-    for (int j = 0; j < SEL_ITEMS; ++j) {
-      const bool live = ib + j < n;
+    for (int j = 0; j < SEL_OUT_UNROLL; ++j) {
+      const bool live = i0 + 32 * j + lane < w1;
+      cg += __popc(__ballot_sync(0xffffffffu, live && (ge_mode ? (kk[j] >= tau) : (kk[j] > tau))));
+      ce += __popc(__ballot_sync(0xffffffffu, live && !ge_mode && kk[j] == tau));
+    }
+  }
+  if (lane == 0) {
+    s_wgt[warp] = cg;
+    s_weq[warp] = ce;
+  }
+  __syncthreads();
+  int gtb = 0, eqb = 0;
+  for (int w = 0; w < warp; ++w) {
+    gtb += s_wgt[w];
+    eqb += s_weq[w];
+  }
+  for (int i0 = w0; i0 < w1; i0 += 32 * SEL_OUT_UNROLL) {
+    uint32_t kk[SEL_OUT_UNROLL];
+    int id[SEL_OUT_UNROLL];
+#pragma unroll
+    for (int j = 0; j < SEL_OUT_UNROLL; ++j) {  // independent loads first
+      const int i = i0 + 32 * j + lane;
+      kk[j] = i < w1 ? K[i] : 0u;
+      id[j] = i < w1 ? __ldg(src + i) : -1;
+    }
+#pragma unroll
+    for (int j = 0; j < SEL_OUT_UNROLL; ++j) {
+      const bool live = i0 + 32 * j + lane < w1;
       const bool gt = live && (ge_mode ? (kk[j] >= tau) : (kk[j] > tau));
       const bool eq = live && !ge_mode && kk[j] == tau;
-      gt_bits |= static_cast<unsigned>(gt) << j;
-      eq_bits |= static_cast<unsigned>(eq) << j;
-      cg += gt;
-      ce += eq;
+      const unsigned bg = __ballot_sync(0xffffffffu, gt);
+      const unsigned be = __ballot_sync(0xffffffffu, eq);
+      const int my_gt = gtb + __popc(bg & lt_mask);
+      const int my_eq = eqb + __popc(be & lt_mask);
+      if (gt || (eq && my_eq < want)) {
+        const int pos = my_gt + min(my_eq, want);
+        if (pos < q_out) out[pos] = id[j];
+      }
+      gtb += __popc(bg);
+      eqb += __popc(be);
     }
-    const int excl = block_exclusive_scan_1024(cg | (ce << 16), s_warp, &s_total);
-    const int tot = s_total;
-    const int eq_left = max(0, want - run_eq);
-    int gtb = excl & 0xFFFF, eqb = excl >> 16;
-#pragma unroll
-    for (int j = 0; j < SEL_ITEMS; ++j) {
-      const bool gt = (gt_bits >> j) & 1u, eq = (eq_bits >> j) & 1u;
-      const bool sel = gt || (eq && eqb < eq_left);
-      const int pos = run_out + gtb + min(eqb, eq_left);
-      if (sel && pos < q_out) out[pos] = id[j];
-      gtb += gt;
-      eqb += eq;
-    }
-    run_out += (tot & 0xFFFF) + min(tot >> 16, eq_left);
-    run_eq += tot >> 16;
   }
 }
 
@@ -247,7 +378,7 @@ extern "C" lrm_status lrm_select(lrm_ctx* ctx, const float* score, const int32_t
     if (p != nullptr && !aligned(p, 4)) return LRM_ERR_ALIGN;
   DeviceGuard guard(ctx->device);
   if (!guard.ok) return LRM_ERR_CUDA;
-  const size_t smem = SEL_SMEM_KEYS * sizeof(uint32_t);
+  const size_t smem = (SEL_SMEM_KEYS + SEL_CAND_KEYS) * sizeof(uint32_t);
   static thread_local int configured_device = -1;
   if (configured_device != ctx->device) {
     LRM_CHECK_CUDA(

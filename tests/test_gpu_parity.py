@@ -183,3 +183,22 @@ def test_empty_batch():
     assert gpu["flags"] == 0
     assert np.all(gpu["sel_offsets"] == 0)
     assert np.all(gpu["dW"] == 0)
+
+
+@pytest.mark.parametrize("T,E,mode,seed", [(6000, 1, "equal", 13), (20000, 1, "equal", 14),
+                                           (16384, 2, "few", 15), (30000, 4, "few", 16),
+                                           (40000, 2, "spread", 17)])
+def test_large_experts_sampled_bracket_and_fallback(T, E, mode, seed):
+    """Experts with thousands of candidates go through the sampled bracket
+    (and its fallback when the bracket holds too many keys, e.g. all equal)."""
+    inp = custom_inputs(T=T, E=E, k=1, h=64, I=32, s=0.0, rho=Fraction(3, 4), seed=seed)
+    rng = np.random.default_rng(seed)
+    if mode == "equal":
+        inp.g[:] = inp.g[0]
+        inp.phi[:] = inp.phi[0]
+        inp.alpha[:] = np.float32(0.5)
+    elif mode == "few":
+        inp.phi[:] = inp.phi[rng.integers(0, 5, size=inp.phi.shape[0])]
+        inp.g[:] = inp.g[rng.integers(0, 3, size=inp.g.shape[0])]
+        inp.alpha[:] = np.float32(0.25)
+    full_check(inp)
