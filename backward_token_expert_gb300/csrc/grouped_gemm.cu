@@ -34,9 +34,7 @@
 namespace lrm {
 namespace {
 
-constexpr int BK = 64;
 constexpr int MAX_E = 1024;
-constexpr uint32_t ATOM_BYTES = 64 * 64 * 2;  // one [64][64] bf16 swizzle box
 
 // ---------------------------------------------------------------------------
 // wgrad on CTA pairs: dW_e [h, I] in 256 x BN output tiles, one per cluster of
@@ -64,17 +62,49 @@ constexpr uint32_t ATOM_BYTES = 64 * 64 * 2;  // one [64][64] bf16 swizzle box
 
 template <int BN>
 struct CfgPair {
-  static constexpr int A_BYTES = 128 * BK * 2;       // this CTA's 128 rows of M
-  static constexpr int B_BYTES = (BN / 2) * BK * 2;  // this CTA's BN/2 columns of N
+  static constexpr int BKS = 96;                       // K rows per stage: 6 MMAs per barrier round
+  static constexpr int ATOM = 64 * BKS * 2;             // one [BKS][64] bf16 swizzle atom
+  static constexpr int A_BYTES = 2 * ATOM;              // this CTA's 128 rows of M
+  static constexpr int B_BYTES = (BN / 128) * ATOM;     // this CTA's BN/2 columns of N
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = 5;
+  static constexpr int STAGES = 4;
   static constexpr int TMEM_COLS = 2 * BN;
   static constexpr int EPI_WARPS = 8;                       // two per TMEM lane quarter
   static constexpr int THREADS = 64 + 32 * EPI_WARPS + 32;  // + the tail fixer warp
   static constexpr int FIXER_WARP = 2 + EPI_WARPS;
-  static constexpr int STAGING_BYTES = EPI_WARPS * 32 * 128;  // one [32][32] fp32 store box per epilogue warp
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STAGING_BYTES + 1024;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
 };
+
+// In-register transpose for the wgrad epilogue.  r holds one accumulator row
+// (lane = row within the warp's 32) as eight 16-byte quads, slot 4 beta + s =
+// columns 16 beta + 4 s.  Within each group of four lanes the 4 x 4 matrix of
+// quads (row i, slot s) is transposed for each beta by two butterfly stages
+// (stage b swaps bit b of the lane and of the slot), so that afterwards lane i
+// holds, in slot 4 beta + rho, quad s = i of row rho of its group.
+__device__ __forceinline__ void quad_transpose_4x4(uint32_t (&r)[32], int lane) {
+#pragma unroll
+  for (int b = 0; b < 2; ++b) {
+    const bool hi = (lane >> b) & 1;
+#pragma unroll
+    for (int beta = 0; beta < 2; ++beta) {
+#pragma unroll
+      for (int other = 0; other < 2; ++other) {
+        // the slot pair that differs in bit b; the other bit is `other`
+        const int s0 = 4 * beta + (b == 0 ? 2 * other : other);
+        const int s1 = s0 + (1 << b);
+#pragma unroll
+        for (int f = 0; f < 4; ++f) {
+          const uint32_t send = hi ? r[4 * s0 + f] : r[4 * s1 + f];
+          const uint32_t got = __shfl_xor_sync(0xffffffffu, send, 1 << b);
+          if (hi)
+            r[4 * s0 + f] = got;
+          else
+            r[4 * s1 + f] = got;
+        }
+      }
+    }
+  }
+}
 
 // Start row and length of expert e's segment, clamped to the buffers.
 __device__ __forceinline__ void segment(const int32_t* __restrict__ sel_offsets, int e, int max_rows, int& start,
@@ -117,9 +147,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CfgPair<BN>::THREADS
   const int per_expert = tiles_m * tiles_n;
   const int total_tiles = E * per_expert;
 
-  // Schedule: the pair tiles of all experts, heaviest expert first, dealt to
-  // the pairs in a snake order (round r goes forward for even r, backward for
-  // odd r), which balances the ragged K loops across pairs.
+  // Schedule: the pair tiles of all experts, heaviest expert first, cut into
+  // blocks of one tile per pair.  Rounds alternate between the heavy front
+  // and the light back of that list (blocks 0, last, 1, last - 1, ...), so the
+  // long K loops of heavy tiles overlap the dW stores of light ones, and the
+  // tiles of one expert still run side by side (their operands are shared
+  // through L2).  Within a block the deal is a snake (forward for even
+  // blocks, backward for odd ones), which balances the ragged K loops.
   for (int e = tid; e < E; e += C::THREADS) {
     int st, ln;
     segment(sel_offsets, e, max_rows, st, ln);
@@ -164,7 +198,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CfgPair<BN>::THREADS
     *abort_flag = 1;
     raise_flag(status, LRM_ERR_TIMEOUT);
   };
-  auto tile_of = [&](int round) { return round * npairs + ((round & 1) ? npairs - 1 - pair : pair); };
+  const int nblocks = (total_tiles + npairs - 1) / npairs;
+  auto tile_of = [&](int round) {
+    const int b = (round & 1) ? nblocks - 1 - (round >> 1) : (round >> 1);
+    return b * npairs + ((b & 1) ? npairs - 1 - pair : pair);
+  };
   auto decode = [&](int tile, int& e, int& mt, int& nt) {
     const int slot = tile / per_expert;
     e = s_order[slot];
@@ -181,12 +219,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CfgPair<BN>::THREADS
       const uint32_t full0 = mapa_shared(&full_bar[0], 0);  // the even CTA's full barriers
       uint32_t it = 0, tail_par = 0;
       bool ok = true;
-      for (int round = 0, tile = tile_of(0); tile < total_tiles && ok; tile = tile_of(++round)) {
+      for (int round = 0; round < nblocks && ok; ++round) {
+        const int tile = tile_of(round);
+        if (tile >= total_tiles) continue;
         int e, mt, nt;
         decode(tile, e, mt, nt);
         int start, len;
         segment(sel_offsets, e, max_rows, start, len);
-        const int nkb = (len + BK - 1) / BK;
+        const int nkb = (len + C::BKS - 1) / C::BKS;
         for (int kb = 0; kb < nkb; ++kb, ++it) {
           const uint32_t s = it % C::STAGES;
           const uint32_t ph = (it / C::STAGES) & 1u;
@@ -199,8 +239,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CfgPair<BN>::THREADS
           uint8_t* b_dst = a_dst + C::A_BYTES;
           const int xa = mt * 256 + static_cast<int>(rank) * 128;
           const int xb = nt * BN + static_cast<int>(rank) * (BN / 2);
-          const int y = start + kb * BK;
-          if (len - kb * BK >= BK) {
+          const int y = start + kb * C::BKS;
+          if (len - kb * C::BKS >= C::BKS) {
             if (leader) {
               // both arrivals of a full block come from here; the odd CTA's
               // loads only add their bytes
@@ -209,16 +249,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CfgPair<BN>::THREADS
             }
             const uint32_t bar = full0 + s * 8;
 #pragma unroll
-            for (int c = 0; c < 2; ++c) tma_load_2d_pair(a_dst + c * ATOM_BYTES, &tmA, bar, xa + c * 64, y);
+            for (int c = 0; c < 2; ++c) tma_load_2d_pair(a_dst + c * C::ATOM, &tmA, bar, xa + c * 64, y);
 #pragma unroll
-            for (int c = 0; c < BN / 128; ++c) tma_load_2d_pair(b_dst + c * ATOM_BYTES, &tmB, bar, xb + c * 64, y);
+            for (int c = 0; c < BN / 128; ++c) tma_load_2d_pair(b_dst + c * C::ATOM, &tmB, bar, xb + c * 64, y);
           } else {
             mbar_arrive_expect_tx(&tail_bar[s], C::STAGE_BYTES);
 #pragma unroll
-            for (int c = 0; c < 2; ++c) tma_load_2d(a_dst + c * ATOM_BYTES, &tmA, &tail_bar[s], xa + c * 64, y);
+            for (int c = 0; c < 2; ++c) tma_load_2d(a_dst + c * C::ATOM, &tmA, &tail_bar[s], xa + c * 64, y);
 #pragma unroll
             for (int c = 0; c < BN / 128; ++c)
-              tma_load_2d(b_dst + c * ATOM_BYTES, &tmB, &tail_bar[s], xb + c * 64, y);
+              tma_load_2d(b_dst + c * C::ATOM, &tmB, &tail_bar[s], xb + c * 64, y);
             tail_par ^= 1u << s;
           }
         }
@@ -235,12 +275,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CfgPair<BN>::THREADS
     constexpr uint32_t idesc = idesc_bf16_f32(256, BN, 1u, 1u);
     uint32_t it = 0, acc_it = 0;
     bool ok = leader;
-    for (int round = 0, tile = tile_of(0); tile < total_tiles && ok; tile = tile_of(++round)) {
+    for (int round = 0; round < nblocks && ok; ++round) {
+      const int tile = tile_of(round);
+      if (tile >= total_tiles) continue;
       int e, mt, nt;
       decode(tile, e, mt, nt);
       int start, len;
       segment(sel_offsets, e, max_rows, start, len);
-      const int nkb = (len + BK - 1) / BK;
+      const int nkb = (len + C::BKS - 1) / C::BKS;
       if (nkb == 0) continue;
       const uint32_t acc = acc_it & 1u;
       const uint32_t aph = (acc_it >> 1) & 1u;
@@ -253,9 +295,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CfgPair<BN>::THREADS
       for (int kb = 0; kb < nkb; ++kb, ++it) {
         const uint32_t s = it % C::STAGES;
         const uint32_t ph = (it / C::STAGES) & 1u;
-        const int valid = len - kb * BK;
-        const bool tail = valid < BK;
-        const int nk = tail ? (valid + 15) / 16 : BK / 16;
+        const int valid = len - kb * C::BKS;
+        const bool tail = valid < C::BKS;
+        const int nk = tail ? (valid + 15) / 16 : C::BKS / 16;
         // a tail stage was zero-filled by the fixer warps of both CTAs
         const bool got = tail ? mbar_wait_cluster(&full_bar[s], ph, budget_ns, abort_flag)
                               : mbar_wait(&full_bar[s], ph, budget_ns, abort_flag);
@@ -267,11 +309,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CfgPair<BN>::THREADS
         tc_fence_after();
         if (lane == 0) {
           const uint32_t a_addr = smem_u32(smem + s * C::STAGE_BYTES);
-          const uint32_t b_addr = a_addr + C::A_BYTES;
-          for (int kk = 0; kk < nk; ++kk) {
-            const uint64_t adesc = smem_desc_sw128(a_addr + kk * 2048, ATOM_BYTES, 1024);
-            const uint64_t bdesc = smem_desc_sw128(b_addr + kk * 2048, ATOM_BYTES, 1024);
-            mma_bf16_ss_pair(d_tmem, adesc, bdesc, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          const uint64_t adesc = smem_desc_sw128(a_addr, C::ATOM, 1024);
+          const uint64_t bdesc = smem_desc_sw128(a_addr + C::A_BYTES, C::ATOM, 1024);
+          // a K step of 16 rows is 2048 bytes, 128 in the descriptor's address field; the
+          // MMAs of a full stage are issued back to back (the tensor pipe queues few)
+          if (!tail) {
+#pragma unroll
+            for (int kk = 0; kk < C::BKS / 16; ++kk)
+              mma_bf16_ss_pair(d_tmem, adesc + kk * 128, bdesc + kk * 128, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          } else {
+            for (int kk = 0; kk < nk; ++kk)
+              mma_bf16_ss_pair(d_tmem, adesc + kk * 128, bdesc + kk * 128, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
           }
           mma_commit_pair_multicast(&empty_bar[s]);
         }
@@ -294,16 +342,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CfgPair<BN>::THREADS
     const uint32_t full0 = mapa_shared(&full_bar[0], 0);
     uint32_t it = 0, tail_par = 0;
     bool ok = true;
-    for (int round = 0, tile = tile_of(0); tile < total_tiles && ok; tile = tile_of(++round)) {
+    for (int round = 0; round < nblocks && ok; ++round) {
+      const int tile = tile_of(round);
+      if (tile >= total_tiles) continue;
       int e, mt, nt;
       decode(tile, e, mt, nt);
       int start, len;
       segment(sel_offsets, e, max_rows, start, len);
-      const int nkb = (len + BK - 1) / BK;
+      const int nkb = (len + C::BKS - 1) / C::BKS;
       if (nkb == 0) continue;
       it += nkb - 1;  // full blocks need no fixing
-      const int valid = len - (nkb - 1) * BK;
-      if (valid < BK) {
+      const int valid = len - (nkb - 1) * C::BKS;
+      if (valid < C::BKS) {
         const uint32_t s = it % C::STAGES;
         const uint32_t tph = (tail_par >> s) & 1u;
         tail_par ^= 1u << s;
@@ -321,7 +371,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CfgPair<BN>::THREADS
         for (int i = lane; i < units; i += 32) {
           const int atom = i / (nz * 8);
           const int rem = i - atom * nz * 8;
-          uint8_t* base = atom < 2 ? a_stage + atom * ATOM_BYTES : b_stage + (atom - 2) * ATOM_BYTES;
+          uint8_t* base = atom < 2 ? a_stage + atom * C::ATOM : b_stage + (atom - 2) * C::ATOM;
           *reinterpret_cast<uint4*>(base + (valid + rem / 8) * 128 + (rem % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
         }
         fence_proxy_async_smem();
@@ -340,24 +390,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CfgPair<BN>::THREADS
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;                  // TMEM lane quarter this warp may access
     const int c_begin = ((warp - 2) >> 2) * (BN / 2);  // this warp's half of the columns
-    const int row_in_half = q * 32 + lane;
-    uint8_t* stg = smem + C::STAGES * C::STAGE_BYTES + (warp - 2) * (32 * 128);
+    // store layout: a warp instruction covers 8 rows x 16 columns (64 bytes
+    // of each row); lane = (row within the 8) * 4 + column quad
+    const int sub_row = lane >> 2, quad = (lane & 3) * 4;
     const uint32_t tempty0 = mapa_shared(&tempty_bar[0], 0);
     uint32_t acc_it = 0;
-    for (int round = 0, tile = tile_of(0); tile < total_tiles; tile = tile_of(++round)) {
+    for (int round = 0; round < nblocks; ++round) {
+      const int tile = tile_of(round);
+      if (tile >= total_tiles) continue;
       int e, mt, nt;
       decode(tile, e, mt, nt);
-      const int row0 = mt * 256 + static_cast<int>(rank) * 128;  // first dW row of this CTA's half
+      const int row_w = mt * 256 + static_cast<int>(rank) * 128 + q * 32;  // first dW row of this warp
+      float* obase = out + (static_cast<size_t>(e) * h + row_w) * I;
       int start, len;
       segment(sel_offsets, e, max_rows, start, len);
       if (len == 0) {
         if (!accumulate) {
-          const int i = row0 + row_in_half;
-          if (i < h) {
-            float* orow = out + (static_cast<size_t>(e) * h + i) * I;
-            for (int c = c_begin; c < c_begin + BN / 2; c += 4) {
-              const int col = nt * BN + c;
-              if (col < I) *reinterpret_cast<float4*>(orow + col) = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int c = 0; c < BN / 2; c += 16) {
+            const int col = nt * BN + c_begin + c + quad;
+            if (col >= I) break;
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              const int rr = 8 * v + sub_row;
+              if (row_w + rr < h)
+                *reinterpret_cast<float4*>(obase + static_cast<size_t>(rr) * I + col) =
+                    make_float4(0.f, 0.f, 0.f, 0.f);
             }
           }
         }
@@ -377,32 +434,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CfgPair<BN>::THREADS
       for (int c = 0; c < BN / 2; c += 32) {
         const bool more = c + 32 < BN / 2;
         if (more) tmem_ld_32x32b_x32(taddr + c + 32, nx);  // next chunk in flight while this one is stored
-        const int col0 = nt * BN + c_begin + c;
-        if (!accumulate) {
-          if (lane == 0) bulk_wait_read_all();
-          __syncwarp();
+        // 4 x 4 transpose of 16-byte quads inside each group of four lanes (two
+        // butterfly stages): lane 4g + i then holds, for each row 4g + rho and
+        // 16-column half beta, the quad of columns 16 beta + 4i.
+        quad_transpose_4x4(r, lane);
+        const int col = nt * BN + c_begin + c + 4 * (lane & 3);
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            *reinterpret_cast<uint4*>(stg + lane * 128 + ((j ^ (lane & 7)) << 4)) =
-                make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_3d(&tmOut, stg, col0, row0 + q * 32, e);
-            bulk_commit_group();
-          }
-        } else {
-          const int i = row0 + row_in_half;
-          if (i < h) {
-            float* orow = out + (static_cast<size_t>(e) * h + i) * I;
+        for (int beta = 0; beta < 2; ++beta) {
+          if (col + 16 * beta < I) {
 #pragma unroll
-            for (int v = 0; v < 8; ++v) {
-              const int col = col0 + v * 4;
-              if (col < I) {
-                const float4 o = *reinterpret_cast<const float4*>(orow + col);
-                *reinterpret_cast<float4*>(orow + col) =
-                    make_float4(o.x + __uint_as_float(r[4 * v]), o.y + __uint_as_float(r[4 * v + 1]),
-                                o.z + __uint_as_float(r[4 * v + 2]), o.w + __uint_as_float(r[4 * v + 3]));
+            for (int rho = 0; rho < 4; ++rho) {
+              const int rr = 4 * (lane >> 2) + rho;
+              if (row_w + rr < h) {
+                float4 val = make_float4(__uint_as_float(r[16 * beta + 4 * rho]), __uint_as_float(r[16 * beta + 4 * rho + 1]),
+                                         __uint_as_float(r[16 * beta + 4 * rho + 2]),
+                                         __uint_as_float(r[16 * beta + 4 * rho + 3]));
+                float* o = obase + static_cast<size_t>(rr) * I + col + 16 * beta;
+                if (accumulate) {
+                  const float4 old = *reinterpret_cast<const float4*>(o);
+                  val.x += old.x;
+                  val.y += old.y;
+                  val.z += old.z;
+                  val.w += old.w;
+                }
+                *reinterpret_cast<float4*>(o) = val;
               }
             }
           }
@@ -423,8 +478,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CfgPair<BN>::THREADS
       }
       ++acc_it;
     }
-    if (lane == 0) bulk_wait_all();
-    __syncwarp();
   }
 
   tc_fence_before();
@@ -455,14 +508,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CfgPair<BN>::THREADS
 
 template <int BNR>
 struct CfgDgradPair {
-  static constexpr int A_BYTES = 128 * BK * 2;        // this CTA's 128 I columns of W_e, MN-major
-  static constexpr int B_BYTES = (BNR / 2) * BK * 2;  // this CTA's rows of the segment, K-major
+  static constexpr int BKS = 128;                    // K (= h) per stage: 8 MMAs per barrier round
+  static constexpr int A_ATOM = 64 * BKS * 2;         // [BKS][64] bf16: 64 I columns of W_e, MN-major
+  static constexpr int B_ATOM = (BNR / 2) * 64 * 2;   // [BNR/2][64] bf16: 64 K of this CTA's rows, K-major
+  static constexpr int A_BYTES = 2 * A_ATOM;          // this CTA's 128 I columns
+  static constexpr int B_BYTES = (BKS / 64) * B_ATOM;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = 5;
+  static constexpr int STAGES = 3;
   static constexpr int TMEM_COLS = 2 * BNR;
   static constexpr int EPI_WARPS = 8;
   static constexpr int THREADS = 64 + 32 * EPI_WARPS;
-  static constexpr int T_PITCH = 40;  // bf16 per row of a warp's transpose buffer (80 B: spreads banks)
+  static constexpr int T_PITCH = 32;  // bf16 per row of a warp's transpose buffer (64 B; 16-byte chunks XOR-swizzled)
   static constexpr int STAGING_BYTES = EPI_WARPS * 32 * T_PITCH * 2;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STAGING_BYTES + 1024;
 };
@@ -483,7 +539,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CfgDgradPair<BNR>::T
   __shared__ __align__(8) uint64_t drain_bar;
   __shared__ uint32_t s_tmem_base;
   __shared__ int s_abort;
-  __shared__ int s_prefix[MAX_E + 1];  // first pair tile of every expert
+  __shared__ int s_len[MAX_E];
+  __shared__ uint16_t s_order[MAX_E];  // experts by descending retained rows (ties: lower id)
+  __shared__ int s_prefix[MAX_E + 1];  // first pair tile of the expert at each position of s_order
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = cluster_ctarank();
@@ -491,16 +549,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CfgDgradPair<BNR>::T
   const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
   const int tiles_m = (I + 255) / 256;  // pair tiles over the expert width
 
-  if (warp == 0) {
-    // pair tiles per expert: ceil(len / BNR) x tiles_m (32 experts per lane, then a warp scan)
-    const int per = (E + 31) / 32;
-    const int e0 = lane * per;
-    int local = 0;
-    for (int e = e0; e < min(E, e0 + per); ++e) {
-      int st, ln;
-      segment(sel_offsets, e, max_rows, st, ln);
-      local += ((ln + BNR - 1) / BNR) * tiles_m;
+  // Schedule: experts heaviest first (so the short tiles of light experts
+  // even out the end), the tiles of one expert side by side (they share W_e
+  // through L2), dealt round robin to the pairs.
+  for (int e = tid; e < E; e += C::THREADS) {
+    int st, ln;
+    segment(sel_offsets, e, max_rows, st, ln);
+    s_len[e] = ln;
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += C::THREADS) {
+    const int le = s_len[e];
+    int pos = 0;
+    for (int x = 0; x < E; ++x) {
+      const int lx = s_len[x];
+      pos += (lx > le) || (lx == le && x < e);
     }
+    s_order[pos] = static_cast<uint16_t>(e);
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // pair tiles per expert: ceil(len / BNR) x tiles_m (a run of positions per lane, then a warp scan)
+    const int per = (E + 31) / 32;
+    const int i0 = lane * per;
+    int local = 0;
+    for (int i = i0; i < min(E, i0 + per); ++i) local += ((s_len[s_order[i]] + BNR - 1) / BNR) * tiles_m;
     int incl = local;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -508,11 +581,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CfgDgradPair<BNR>::T
       if (lane >= o) incl += y;
     }
     int run = incl - local;
-    for (int e = e0; e < min(E, e0 + per); ++e) {
-      int st, ln;
-      segment(sel_offsets, e, max_rows, st, ln);
-      s_prefix[e] = run;
-      run += ((ln + BNR - 1) / BNR) * tiles_m;
+    for (int i = i0; i < min(E, i0 + per); ++i) {
+      s_prefix[i] = run;
+      run += ((s_len[s_order[i]] + BNR - 1) / BNR) * tiles_m;
     }
     if (lane == 31) s_prefix[E] = incl;
   }
@@ -547,7 +618,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CfgDgradPair<BNR>::T
   };
   // tile -> expert, row tile nt (over the segment), width tile mt (over I)
   auto decode = [&](int tile, int& e, int& nt, int& mt) {
-    int lo = 0, hi = E - 1;  // last e with s_prefix[e] <= tile
+    int lo = 0, hi = E - 1;  // last position with s_prefix <= tile
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
       if (s_prefix[mid] <= tile)
@@ -555,7 +626,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CfgDgradPair<BNR>::T
       else
         hi = mid - 1;
     }
-    e = lo;
+    e = s_order[lo];
     const int rem = tile - s_prefix[lo];
     nt = rem / tiles_m;
     mt = rem - nt * tiles_m;
@@ -563,7 +634,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CfgDgradPair<BNR>::T
   // rows of row tile nt that the MMA computes: the remainder rounded up to 32
   // (N of a pair MMA with M = 256 is a multiple of 32)
   auto tile_rows = [&](int len, int nt) { return min(BNR, ((len - nt * BNR + 31) / 32) * 32); };
-  const int nkb = (h + BK - 1) / BK;
+  const int nkb = (h + C::BKS - 1) / C::BKS;  // K past h reads as zeros (tensor bounds)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -597,8 +668,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CfgDgradPair<BNR>::T
           }
           const uint32_t bar = full0 + s * 8;
 #pragma unroll
-          for (int c = 0; c < 2; ++c) tma_load_3d_pair(a_dst + c * ATOM_BYTES, &tmA, bar, xa + c * 64, kb * BK, e);
-          tma_load_2d_pair(b_dst, &tmB, bar, kb * BK, yb);
+          for (int c = 0; c < 2; ++c) tma_load_3d_pair(a_dst + c * C::A_ATOM, &tmA, bar, xa + c * 64, kb * C::BKS, e);
+#pragma unroll
+          for (int c = 0; c < C::BKS / 64; ++c) tma_load_2d_pair(b_dst + c * C::B_ATOM, &tmB, bar, kb * C::BKS + c * 64, yb);
         }
       }
       // the even CTA's commits arrive on these barriers asynchronously: wait
@@ -636,13 +708,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CfgDgradPair<BNR>::T
         tc_fence_after();
         if (lane == 0) {
           const uint32_t a_addr = smem_u32(smem + s * C::STAGE_BYTES);
-          const uint32_t b_addr = a_addr + C::A_BYTES;
+          const uint64_t adesc = smem_desc_sw128(a_addr, C::A_ATOM, 1024);
+          const uint64_t bdesc = smem_desc_sw128(a_addr + C::A_BYTES, 16, 1024);
+          // descriptor address field in 16-byte units: A (MN-major) advances 2048 B per
+          // 16 K rows; B (K-major) 32 B per 16 K inside an atom, then the next atom
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t adesc = smem_desc_sw128(a_addr + kk * 2048, ATOM_BYTES, 1024);  // MN-major: 16 K rows
-            const uint64_t bdesc = smem_desc_sw128(b_addr + kk * 32, 16, 1024);            // K-major: 32 B per K step
-            mma_bf16_ss_pair(d_tmem, adesc, bdesc, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
-          }
+          for (int kk = 0; kk < C::BKS / 16; ++kk)
+            mma_bf16_ss_pair(d_tmem, adesc + kk * 128, bdesc + (kk >> 2) * (C::B_ATOM >> 4) + (kk & 3) * 2, idesc,
+                             (kb > 0 || kk > 0) ? 1u : 0u);
           mma_commit_pair_multicast(&empty_bar[s]);
         }
         __syncwarp();
@@ -691,8 +764,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CfgDgradPair<BNR>::T
         __syncwarp();  // the previous chunk's reads of the buffer are done
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
+          // row j, I column `lane`: 16-byte chunk lane / 8 of the row, XOR-swizzled by row
           const __nv_bfloat16 b = __float2bfloat16_rn(__uint_as_float(r[j]));
-          tbuf[j * C::T_PITCH + lane] = *reinterpret_cast<const uint16_t*>(&b);
+          tbuf[j * C::T_PITCH + ((((lane >> 3) ^ (j >> 1)) & 3) << 3) + (lane & 7)] =
+              *reinterpret_cast<const uint16_t*>(&b);
         }
         __syncwarp();
         if (c + lane < rows_valid) {  // lane = output row c + lane
@@ -700,7 +775,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CfgDgradPair<BNR>::T
           uint16_t* orow = obase + static_cast<size_t>(c + lane) * I;
 #pragma unroll
           for (int v = 0; v < 4; ++v)
-            if (col0 + v * 8 < I) *reinterpret_cast<uint4*>(orow + v * 8) = src[v];
+            if (col0 + v * 8 < I) *reinterpret_cast<uint4*>(orow + v * 8) = src[(v ^ (lane >> 1)) & 3];
         }
       }
       tc_fence_before();
@@ -735,11 +810,12 @@ lrm_status encode_2d(lrm_ctx* ctx, CUtensorMap* map, const void* base, uint64_t 
   return r == CUDA_SUCCESS ? LRM_OK : LRM_ERR_CUDA;
 }
 
-// W [E][h][I] bf16 as a 3-D tensor (I, h, E) with [1][64][64] boxes.
-lrm_status encode_w(lrm_ctx* ctx, CUtensorMap* map, const void* base, uint64_t I, uint64_t h, uint64_t E) {
+// W [E][h][I] bf16 as a 3-D tensor (I, h, E) with [1][box_h][64] boxes.
+lrm_status encode_w(lrm_ctx* ctx, CUtensorMap* map, const void* base, uint64_t I, uint64_t h, uint64_t E,
+                    uint32_t box_h) {
   const cuuint64_t dims[3] = {I, h, E};
   const cuuint64_t strides[2] = {I * 2, h * I * 2};
-  const cuuint32_t box[3] = {64, 64, 1};
+  const cuuint32_t box[3] = {64, box_h, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = ctx->encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
                                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -830,8 +906,9 @@ extern "C" lrm_status lrm_grouped_dgrad(lrm_ctx* ctx, const uint16_t* delta_c, c
   DeviceGuard guard(ctx->device);
   if (!guard.ok) return LRM_ERR_CUDA;
   alignas(64) CUtensorMap ma, mb;
-  if ((st = encode_2d(ctx, &ma, delta_c, dims.h, max_rows, 128)) != LRM_OK) return st;
-  if ((st = encode_w(ctx, &mb, W, dims.I, dims.h, dims.E)) != LRM_OK) return st;
+  using CD = CfgDgradPair<256>;
+  if ((st = encode_2d(ctx, &ma, delta_c, dims.h, max_rows, 256 / 2)) != LRM_OK) return st;
+  if ((st = encode_w(ctx, &mb, W, dims.I, dims.h, dims.E, CD::BKS)) != LRM_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   return launch_dgrad_pair<256>(ctx, mb, ma, sel_offsets, dims, max_rows, dphi_c, s);
 }
@@ -854,8 +931,8 @@ extern "C" lrm_status lrm_grouped_wgrad(lrm_ctx* ctx, const uint16_t* delta_c, c
   const void* b_base = max_rows > 0 ? static_cast<const void*>(phi_c) : static_cast<const void*>(dW);
   const uint64_t rows = max_rows > 0 ? static_cast<uint64_t>(max_rows) : 1;
   alignas(64) CUtensorMap ma, mb, mo;
-  if ((st = encode_2d(ctx, &ma, a_base, dims.h, rows, 64)) != LRM_OK) return st;
-  if ((st = encode_2d(ctx, &mb, b_base, dims.I, rows, 64)) != LRM_OK) return st;
+  if ((st = encode_2d(ctx, &ma, a_base, dims.h, rows, CfgPair<256>::BKS)) != LRM_OK) return st;
+  if ((st = encode_2d(ctx, &mb, b_base, dims.I, rows, CfgPair<256>::BKS)) != LRM_OK) return st;
   if ((st = encode_dw(ctx, &mo, dW, dims.I, dims.h, dims.E)) != LRM_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   return launch_wgrad_pair<256>(ctx, ma, mb, mo, sel_offsets, dims, max_rows, accumulate, dW, s);
