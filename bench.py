@@ -145,30 +145,64 @@ class ClockSampler:
 # algorithmic work per launch (bytes or flop)
 
 
-def algorithmic_work(w, retained):
+def algorithmic_work(w, retained, active_experts):
+    """Per launch: (bytes, flop) of the work the method must do.
+
+    Bytes are the HBM traffic a perfect kernel needs (each input read once,
+    each output written once); flop counts only the retained rows, never the
+    padding the method avoids.  A GEMM is bound by whichever roof takes
+    longer: its flop at the bf16 peak or its bytes at the HBM peak.
+    """
     T, E, k, h, I = w.T, w.E, w.k, w.h, w.I
     N = T * k
+    gemm_flop = 2 * retained * h * I
+    rows_bytes = 2 * retained * (h + I)
     return {
-        "route_stats": ("hbm", T * (4 * E + 4 * k) + 4 * N),
-        "score": ("hbm", 2 * T * h + N * (2 * I + 8)),
-        "select": ("hbm", 8 * N + 4 * retained),
-        "compact": ("hbm", retained * (4 * (h + I) + 8)),
-        "dgrad": ("tensor", 2 * retained * h * I),
-        "wgrad": ("tensor", 2 * retained * h * I),
+        "route_stats": (T * (4 * E + 4 * k) + 4 * N, 0),
+        "score": (2 * T * h + N * (2 * I + 8), 0),
+        "select": (8 * N + 4 * retained, 0),
+        "compact": (retained * (4 * (h + I) + 8), 0),
+        "dgrad": (rows_bytes + 2 * active_experts * h * I, gemm_flop),
+        "wgrad": (rows_bytes + 4 * E * h * I, gemm_flop),
     }
 
 
-def roofline_entry(kind, work, ms, pk, sustained):
-    if kind == "hbm":
-        achieved = work / (ms * 1e-3) / 1e9
-        peak = pk["hbm"]
-        unit = "GB/s"
+def roofline_entry(nbytes, flop, ms, pk, sustained):
+    t_hbm = nbytes / (pk["hbm"] * 1e9)
+    tc_peak = pk["bf16_sustained"] if sustained else pk["bf16"]
+    t_tc = flop / (tc_peak * 1e12)
+    sec = ms * 1e-3
+    if t_tc > t_hbm:
+        achieved, peak, unit, kind = flop / sec / 1e12, tc_peak, "TFLOP/s", "tensor"
     else:
-        achieved = work / (ms * 1e-3) / 1e12
-        peak = pk["bf16_sustained"] if sustained else pk["bf16"]
-        unit = "TFLOP/s"
-    return {"bound": kind, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
-            "frac": round(achieved / peak, 4)}
+        achieved, peak, unit, kind = nbytes / sec / 1e9, pk["hbm"], "GB/s", "hbm"
+    ent = {"bound": kind, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+           "frac": round(achieved / peak, 4), "hbm_frac": round(t_hbm / sec, 4), "bytes": nbytes}
+    if flop:
+        ent.update(tensor_frac=round(t_tc / sec, 4), flop=flop)
+    return ent
+
+
+def measured_traffic(kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if the
+    kernel's source has not changed since the counters were taken."""
+    import hashlib
+
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(kernel)
+    except (OSError, ValueError):
+        return None
+    if not rec:
+        return None
+    src = os.path.join(ROOT, rec["source"])
+    try:
+        with open(src, "rb") as f:
+            digest = hashlib.sha256(f.read()).hexdigest()
+    except OSError:
+        return None
+    return rec["dram_bytes"] if digest == rec["source_sha256"] else None
 
 
 # ---------------------------------------------------------------------------
@@ -258,19 +292,22 @@ def run_ours(args, rank, world, local):
     result = None
     if rank == 0:
         pk = peaks()
-        work = algorithmic_work(w, retained)
+        so = rec.buf.sel_offsets.cpu().numpy()
+        active = int((np.diff(so) > 0).sum())
+        work = algorithmic_work(w, retained, active)
         kernels = {}
         for name in KERNELS:
             ms = statistics.mean(per[name])
-            kind, wk = work[name]
-            ent = roofline_entry(kind, wk, ms, pk, sustained=True)
-            ent.update(ms=round(ms, 5), work=wk, work_unit="bytes" if kind == "hbm" else "flop",
-                       share=round(sum(per[name]) / sum(sum(v) for v in per.values()), 4))
+            nbytes, flop = work[name]
+            ent = roofline_entry(nbytes, flop, ms, pk, sustained=True)
+            ent.update(ms=round(ms, 5), share=round(sum(per[name]) / sum(sum(v) for v in per.values()), 4))
             kernels[name] = ent
         dominant = max(KERNELS, key=lambda n: kernels[n]["ms"])
         top = {k2: kernels[dominant][k2] for k2 in ("bound", "achieved", "peak", "unit", "frac")}
-        top.update(kernel=dominant, traffic=None, peak_kind="sustained bf16 (of measured)"
-                   if top["bound"] == "tensor" else "hbm copy (of measured)", peak_source=pk["source"])
+        top.update(kernel=dominant, traffic=measured_traffic(dominant) if w.name == DEFAULT_WORKLOAD else None,
+                   algorithmic_bytes=kernels[dominant]["bytes"],
+                   peak_kind="sustained bf16 (of measured)" if top["bound"] == "tensor" else "hbm copy (of measured)",
+                   peak_source=pk["source"])
         value = world * retained * K / (total_ms * 1e-3)
         result = {
             "metric": METRIC,
