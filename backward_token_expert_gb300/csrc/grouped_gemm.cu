@@ -119,7 +119,7 @@ __device__ __forceinline__ void segment(const int32_t* __restrict__ sel_offsets,
 template <int BN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CfgPair<BN>::THREADS, 1)
     wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                      const __grid_constant__ CUtensorMap tmOut, const int32_t* __restrict__ sel_offsets, int E,
+                      const int32_t* __restrict__ sel_offsets, int E,
                       int h, int I, int max_rows, int accumulate, float* __restrict__ out, unsigned int* status,
                       unsigned long long budget_ns) {
   using C = CfgPair<BN>;
@@ -823,20 +823,8 @@ lrm_status encode_w(lrm_ctx* ctx, CUtensorMap* map, const void* base, uint64_t I
   return r == CUDA_SUCCESS ? LRM_OK : LRM_ERR_CUDA;
 }
 
-// dW [E][h][I] fp32 as a 3-D tensor (I, h, E) with [1][32][32] boxes, 128-byte swizzle.
-lrm_status encode_dw(lrm_ctx* ctx, CUtensorMap* map, const void* base, uint64_t I, uint64_t h, uint64_t E) {
-  const cuuint64_t dims[3] = {I, h, E};
-  const cuuint64_t strides[2] = {I * 4, h * I * 4};
-  const cuuint32_t box[3] = {32, 32, 1};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = ctx->encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides,
-                                 box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                                 CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? LRM_OK : LRM_ERR_CUDA;
-}
-
 template <int BN>
-lrm_status launch_wgrad_pair(lrm_ctx* ctx, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
+lrm_status launch_wgrad_pair(lrm_ctx* ctx, const CUtensorMap& a, const CUtensorMap& b,
                              const int32_t* sel_offsets, const lrm_dims& d, int max_rows, int accumulate, float* out,
                              cudaStream_t s) {
   using C = CfgPair<BN>;
@@ -856,7 +844,7 @@ lrm_status launch_wgrad_pair(lrm_ctx* ctx, const CUtensorMap& a, const CUtensorM
     clusters = n;
     configured_device = ctx->device;
   }
-  kern<<<2 * clusters, C::THREADS, C::SMEM_BYTES, s>>>(a, b, o, sel_offsets, d.E, d.h, d.I, max_rows, accumulate,
+  kern<<<2 * clusters, C::THREADS, C::SMEM_BYTES, s>>>(a, b, sel_offsets, d.E, d.h, d.I, max_rows, accumulate,
                                                          out, ctx->d_status, ctx->wait_budget_ns);
   return launch_status();
 }
@@ -930,10 +918,9 @@ extern "C" lrm_status lrm_grouped_wgrad(lrm_ctx* ctx, const uint16_t* delta_c, c
   const void* a_base = max_rows > 0 ? static_cast<const void*>(delta_c) : static_cast<const void*>(dW);
   const void* b_base = max_rows > 0 ? static_cast<const void*>(phi_c) : static_cast<const void*>(dW);
   const uint64_t rows = max_rows > 0 ? static_cast<uint64_t>(max_rows) : 1;
-  alignas(64) CUtensorMap ma, mb, mo;
+  alignas(64) CUtensorMap ma, mb;
   if ((st = encode_2d(ctx, &ma, a_base, dims.h, rows, CfgPair<256>::BKS)) != LRM_OK) return st;
   if ((st = encode_2d(ctx, &mb, b_base, dims.I, rows, CfgPair<256>::BKS)) != LRM_OK) return st;
-  if ((st = encode_dw(ctx, &mo, dW, dims.I, dims.h, dims.E)) != LRM_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return launch_wgrad_pair<256>(ctx, ma, mb, mo, sel_offsets, dims, max_rows, accumulate, dW, s);
+  return launch_wgrad_pair<256>(ctx, ma, mb, sel_offsets, dims, max_rows, accumulate, dW, s);
 }

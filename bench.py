@@ -37,6 +37,9 @@ DEFAULT_WORKLOAD = "qwen3_30b_a3b_T32768_E128_k8_h2048_I768"
 METRIC = "retained pairs/s through score->select->compact->grouped GEMM"
 UNIT = "pairs/s"
 KERNELS = ("route_stats", "score", "select", "compact", "dgrad", "wgrad")
+# kernels of one step: route stats 3 (count, finalize, scatter), score 1,
+# select 2 (gather, select), compact 1, dgrad 1, wgrad 1
+LAUNCHES_PER_STEP = 9
 
 
 def parse():
@@ -214,6 +217,7 @@ def run_ours(args, rank, world, local):
 
     from backward_token_expert_gb300 import build as B
     from backward_token_expert_gb300.pipeline import Recalibration, to_device_inputs
+    from backward_token_expert_gb300.replicas import job_totals, replica_seed
     from workloads import generate, get_workload
 
     torch.cuda.set_device(local)
@@ -227,8 +231,8 @@ def run_ours(args, rank, world, local):
     if dist:
         dist.barrier()
 
-    # independent replicas: rank r draws its own layer batch (seed r)
-    w = get_workload(args.workload, seed=rank)
+    # independent replicas: rank r draws its own layer batch
+    w = get_workload(args.workload, seed=replica_seed(rank))
     inp = generate(w)
     rec = Recalibration(w.T, w.E, w.k, w.h, w.I, w.cf, w.rho, device=local)
     d = to_device_inputs(inp, f"cuda:{local}")
@@ -281,10 +285,9 @@ def run_ours(args, rank, world, local):
         dist.barrier()
     total_ms = evs[0][0].elapsed_time(evs[-1][6])
     per = {name: [evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K)] for j, name in enumerate(KERNELS)}
-    if dist:
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    # whole job: pairs of every replica over the slowest replica's time
+    job_pairs, job_s = job_totals(retained * K, total_ms * 1e-3, device=f"cuda:{local}")
+    total_ms = job_s * 1e3
     flags = rec.device_status()
     if flags:
         raise RuntimeError(f"device status flags {flags:#x} after the timed steps")
@@ -308,7 +311,7 @@ def run_ours(args, rank, world, local):
                    algorithmic_bytes=kernels[dominant]["bytes"],
                    peak_kind="sustained bf16 (of measured)" if top["bound"] == "tensor" else "hbm copy (of measured)",
                    peak_source=pk["source"])
-        value = world * retained * K / (total_ms * 1e-3)
+        value = job_pairs / job_s
         result = {
             "metric": METRIC,
             "value": value,
@@ -331,16 +334,21 @@ def run_ours(args, rank, world, local):
             },
             "roofline": top,
             "kernels": kernels,
-            "gpu_launches": 8 * K,
+            "gpu_launches": LAUNCHES_PER_STEP * K,
             "host_s": round(t_host, 4),
             "clocks": sampler.summary() if sampler else None,
         }
         if not args.no_comparator:
             result["comparator"] = comparator(rec, d, w, retained, pk)
-        if not args.no_e2e:
-            result["e2e"] = e2e(rec, inp, w, retained, world, min(K, 20))
         if not args.no_cpu_baseline:
-            result["cpu_baseline"] = cpu_baseline(inp, tokens=args.ref_tokens or 4096, steps=2)
+            result["cpu_baseline"] = cpu_baseline(inp, tokens=args.ref_tokens or 8192)
+    if not args.no_e2e:
+        # every replica runs its end-to-end loop at the same time
+        if dist:
+            dist.barrier()
+        ent = e2e(rec, inp, w, retained, min(K, 20), local)
+        if result is not None:
+            result["e2e"] = ent
     rec.close()
     if dist:
         dist.barrier()
@@ -398,7 +406,7 @@ def comparator(rec, d, w, retained, pk, iters=20):
     return out
 
 
-def e2e(rec, inp, w, retained, world, iters):
+def e2e(rec, inp, w, retained, iters, local):
     """Same metric through the public API with host buffers: pinned host->device
     copies of the step's inputs, the path, device->host copies of its results."""
     import torch
@@ -412,7 +420,7 @@ def e2e(rec, inp, w, retained, world, iters):
     h_in = dict(logits=pinned(inp.logits), expert_idx=pinned(inp.expert_idx), alpha=pinned(inp.alpha),
                 g=pinned(inp.g.view(np.int16), torch.bfloat16), phi=pinned(inp.phi.view(np.int16), torch.bfloat16),
                 W=pinned(inp.W.view(np.int16), torch.bfloat16))
-    dev = {k2: torch.empty_like(v, device="cuda") for k2, v in h_in.items()}
+    dev = {k2: torch.empty_like(v, device=f"cuda:{local}") for k2, v in h_in.items()}
     b = rec.buf
     h_out = dict(dW=torch.empty_like(b.dW, device="cpu").pin_memory(),
                  dphi_c=torch.empty_like(b.dphi_c, device="cpu").pin_memory(),
@@ -432,6 +440,8 @@ def e2e(rec, inp, w, retained, world, iters):
         h_out["sel_ids"].copy_(b.sel_ids, non_blocking=True)
         h_out["summary"].copy_(b.summary, non_blocking=True)
 
+    from backward_token_expert_gb300.replicas import job_totals
+
     for _ in range(2):
         one()
     torch.cuda.synchronize()
@@ -440,8 +450,9 @@ def e2e(rec, inp, w, retained, world, iters):
         one()
     torch.cuda.synchronize()
     dt = time.perf_counter() - t0
-    return {"value": world * retained * iters / dt, "unit": UNIT, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": iters, "ms_per_step": dt * 1e3 / iters,
+    pairs, slowest = job_totals(retained * iters, dt, device=f"cuda:{local}")
+    return {"value": pairs / slowest, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": iters, "ms_per_step": slowest * 1e3 / iters,
             "api": "backward_token_expert_gb300.pipeline.Recalibration.run (C ABI), pinned host buffers"}
 
 
@@ -475,9 +486,14 @@ def cpu_cores():
         return os.cpu_count() or 1
 
 
-def cpu_baseline(inp, tokens, steps):
+def cpu_baseline(inp, tokens, target_s=15.0):
+    """The oracle as it stands on a bounded token slice, repeated until about
+    `target_s` seconds of timed CPU work have run (at least two passes)."""
     sl = token_slice(inp, tokens)
-    oracle_step(sl)  # warm-up
+    t0 = time.perf_counter()
+    oracle_step(sl)  # warm-up, also sizes the repetition count
+    first = time.perf_counter() - t0
+    steps = max(2, min(50, int(target_s / max(first, 1e-3))))
     t0 = time.perf_counter()
     retained = 0
     for _ in range(steps):
