@@ -136,8 +136,12 @@ extern "C" lrm_status lrm_compact(lrm_ctx* ctx, const uint16_t* g, const uint16_
     return LRM_ERR_ALIGN;
   DeviceGuard guard(ctx->device);
   if (!guard.ok) return LRM_ERR_CUDA;
+  static thread_local int cap_device = -1, cap = 0;
+  if (cap_device != ctx->device) {
+    cap = resident_grid(ctx, compact_kernel, CP_THREADS, 0);
+    cap_device = ctx->device;
+  }
   const int need = (max_rows + CP_WARPS - 1) / CP_WARPS;
-  const int cap = ctx->sm_count * 8;
   const int grid = need < cap ? need : cap;
   compact_kernel<<<grid, CP_THREADS, 0, static_cast<cudaStream_t>(stream)>>>(
       reinterpret_cast<const uint4*>(g), reinterpret_cast<const uint4*>(phi), alpha, sel_offsets, sel_ids,
@@ -165,7 +169,11 @@ extern "C" lrm_status lrm_compact_padded(lrm_ctx* ctx, const uint16_t* delta_c, 
   const long long slots = static_cast<long long>(dims.E) * C;
   long long need = (slots + CP_WARPS - 1) / CP_WARPS;
   if (need < 1) need = 1;
-  const long long cap = ctx->sm_count * 8;
+  static thread_local int cap_device = -1, cap = 0;
+  if (cap_device != ctx->device) {
+    cap = resident_grid(ctx, compact_padded_kernel, CP_THREADS, 0);
+    cap_device = ctx->device;
+  }
   const int grid = static_cast<int>(need < cap ? need : cap);
   compact_padded_kernel<<<grid, CP_THREADS, 0, static_cast<cudaStream_t>(stream)>>>(
       reinterpret_cast<const uint4*>(delta_c), reinterpret_cast<const uint4*>(phi_c), sel_offsets, dims.E, C,

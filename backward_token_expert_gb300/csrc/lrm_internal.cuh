@@ -58,6 +58,17 @@ struct DeviceGuard {
   }
 };
 
+// Blocks of `kern` that are resident on the context's device at once: the
+// grid of a persistent, grid-stride kernel (a larger grid would leave a
+// partial second wave doing a full share of the work alone).
+template <typename Kern>
+inline int resident_grid(const lrm_ctx* ctx, Kern kern, int threads, size_t dyn_smem) {
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, dyn_smem) != cudaSuccess || per_sm < 1)
+    per_sm = 1;
+  return per_sm * ctx->sm_count;
+}
+
 inline lrm_status launch_status() {
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? LRM_OK : LRM_ERR_CUDA;
