@@ -11,12 +11,14 @@
 //               with shared-memory atomics, and the softmax of each token
 //               (one warp per token, the next token's logits prefetched) is
 //               summed per warp in registers, then per block in a fixed order;
-//   rs_finalize one block: counts, offsets, per-(expert, block) bucket bases,
-//               P, f, quotas and the summary (one warp per expert row of the
-//               expert-major workspace, loads issued eight at a time);
-//   rs_scatter  same chunking as rs_count: stable scatter of pair ids into
-//               the bucket (each warp owns a contiguous sub-range, ranks
-//               inside a warp come from __match_any_sync).
+//   rs_rows     one warp per expert row of the expert-major workspace: n_e,
+//               P_e, f_e, the quota, and per-(expert, block) bucket bases
+//               relative to the expert's start (loads issued eight at a time);
+//   rs_scatter  every block scans the E counts for the expert offsets (block
+//               0 also writes offsets[] and the summary), then, with the same
+//               chunking as rs_count, scatters its pair ids stably into the
+//               bucket (each warp owns a contiguous sub-range, ranks inside a
+//               warp come from __match_any_sync).
 #include <limits.h>
 #include <math.h>
 
@@ -33,7 +35,8 @@ constexpr int RS_THREADS = 512;
 constexpr int RS_WARPS = RS_THREADS / 32;
 constexpr int RS_PAIRS_PER_BLOCK = 1024;
 constexpr int RS_MAX_PER_THREAD = (RS_PAIRS_PER_BLOCK + RS_THREADS - 1) / RS_THREADS;
-constexpr int RS_FIN_THREADS = 1024;
+constexpr int RR_WARPS = 8;  // rs_rows: experts per block, one warp each
+constexpr int RR_THREADS = 32 * RR_WARPS;
 constexpr int FIN_UNROLL = 8;
 
 struct RsLayout {
@@ -148,167 +151,151 @@ __global__ void __launch_bounds__(RS_THREADS) rs_count(const float* __restrict__
   }
 }
 
-__global__ void __launch_bounds__(RS_FIN_THREADS) rs_finalize(
-    int T, int E, int k, int nblk, int32_t cf_num, int32_t cf_den, int32_t rho_num, int32_t rho_den,
-    int32_t* __restrict__ ws_hist, const float* __restrict__ ws_p, int32_t* __restrict__ counts,
-    int32_t* __restrict__ offsets, float* __restrict__ P, float* __restrict__ f, int32_t* __restrict__ quota,
-    lrm_route_summary* __restrict__ summary) {
-  __shared__ int s_warp[32];
-  __shared__ int s_total;
-  __shared__ int s_cnt[1024];
-  __shared__ int s_off[1024];
-  __shared__ float s_P[1024];
-  __shared__ long long s_red_i[6][32];
-  __shared__ float s_red_d[2][32];
-  const int e = threadIdx.x;
-  const int lane = e & 31, warp = e >> 5;
-  const bool live = e < E;
+// One warp per expert row of the expert-major workspace: the routed count,
+// the summed importance, and, in place, the stable-scatter base of every count
+// block relative to the expert's first bucket slot (an exclusive scan along
+// the row).  Writes the per-expert outputs: n_e, P_e, f_e and the quota
+// Q_e = ceil(rho min(n_e, C)) in exact integer arithmetic.
+__global__ void __launch_bounds__(RR_THREADS) rs_rows(int T, int E, int k, int nblk, int32_t cf_num, int32_t cf_den,
+                                                      int32_t rho_num, int32_t rho_den,
+                                                      int32_t* __restrict__ ws_hist, const float* __restrict__ ws_p,
+                                                      int32_t* __restrict__ counts, float* __restrict__ P,
+                                                      float* __restrict__ f, int32_t* __restrict__ quota) {
+  const int lane = threadIdx.x & 31;
+  const int x = blockIdx.x * RR_WARPS + (threadIdx.x >> 5);
+  if (x >= E) return;
   const long long N = static_cast<long long>(T) * k;
-
-  // phase 1: one warp per expert row (expert-major workspace, coalesced)
-  for (int x = warp; x < E; x += RS_FIN_THREADS / 32) {
-    const size_t row = static_cast<size_t>(x) * nblk;
-    int c = 0;
-    float ps = 0.f;
-    for (int b0 = 0; b0 < nblk; b0 += 32 * FIN_UNROLL) {
-      int hv[FIN_UNROLL];
-      float pv[FIN_UNROLL];
+  const size_t row = static_cast<size_t>(x) * nblk;
+  int run = 0;
+  float ps = 0.f;
+  for (int b0 = 0; b0 < nblk; b0 += 32 * FIN_UNROLL) {
+    int hv[FIN_UNROLL];
+    float pv[FIN_UNROLL];
 #pragma unroll
-      for (int j = 0; j < FIN_UNROLL; ++j) {
-        const int b = b0 + lane + 32 * j;
-        hv[j] = b < nblk ? ws_hist[row + b] : 0;
-        pv[j] = b < nblk ? ws_p[row + b] : 0.f;
-      }
-#pragma unroll
-      for (int j = 0; j < FIN_UNROLL; ++j) {
-        c += hv[j];
-        ps += pv[j];
-      }
+    for (int j = 0; j < FIN_UNROLL; ++j) {
+      const int b = b0 + lane + 32 * j;
+      hv[j] = b < nblk ? ws_hist[row + b] : 0;
+      pv[j] = b < nblk ? ws_p[row + b] : 0.f;
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      c += __shfl_xor_sync(0xffffffffu, c, o);
-      ps += __shfl_xor_sync(0xffffffffu, ps, o);
-    }
-    if (lane == 0) {
-      s_cnt[x] = c;
-      s_P[x] = ps;
-    }
-  }
-  __syncthreads();
-  const int cnt = live ? s_cnt[e] : 0;
-  const int off = block_exclusive_scan_1024(cnt, s_warp, &s_total);
-  if (live) {
-    counts[e] = cnt;
-    offsets[e] = off;
-    s_off[e] = off;
-  }
-  if (e == 0) offsets[E] = s_total;
-  __syncthreads();
-  // phase 2: per-(expert, block) base offsets of the stable scatter, in place
-  for (int x = warp; x < E; x += RS_FIN_THREADS / 32) {
-    const size_t row = static_cast<size_t>(x) * nblk;
-    int run = s_off[x];
-    for (int b0 = 0; b0 < nblk; b0 += 32 * FIN_UNROLL) {
-      int hv[FIN_UNROLL];
+    for (int j = 0; j < FIN_UNROLL; ++j) ps += pv[j];
 #pragma unroll
-      for (int j = 0; j < FIN_UNROLL; ++j) {
-        const int b = b0 + lane + 32 * j;
-        hv[j] = b < nblk ? ws_hist[row + b] : 0;
+    for (int j = 0; j < FIN_UNROLL; ++j) {
+      const int b = b0 + lane + 32 * j;
+      int incl = hv[j];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
       }
-#pragma unroll
-      for (int j = 0; j < FIN_UNROLL; ++j) {
-        const int b = b0 + lane + 32 * j;
-        int incl = hv[j];
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int y = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += y;
-        }
-        if (b < nblk) ws_hist[row + b] = run + incl - hv[j];
-        run += __shfl_sync(0xffffffffu, incl, 31);
-      }
+      if (b < nblk) ws_hist[row + b] = run + incl - hv[j];
+      run += __shfl_sync(0xffffffffu, incl, 31);
     }
   }
-
-  // capacity and quota in exact integer arithmetic
-  const long long C = (static_cast<long long>(cf_num) * N) / (static_cast<long long>(cf_den) * E);
-  // fp32 throughout: fp64 runs at a small fraction of the fp32 rate on this part
-  float Pe = 0.f;
-  long long q = 0, drop = 0;
-  if (live) {
-    Pe = (T > 0) ? s_P[e] / static_cast<float>(T) : 0.f;
-    const long long m = cnt < C ? cnt : C;
-    q = (static_cast<long long>(rho_num) * m + rho_den - 1) / rho_den;
-    drop = cnt > C ? cnt - C : 0;
-    P[e] = Pe;
-    f[e] = N > 0 ? static_cast<float>(cnt) / static_cast<float>(N) : 0.f;
-    quota[e] = static_cast<int32_t>(q);
-  }
-  const float fe = (live && N > 0) ? static_cast<float>(cnt) / static_cast<float>(N) : 0.f;
-
-  // deterministic block reductions
-  long long vi[5] = {drop, q, live ? cnt : LLONG_MIN, live ? cnt : LLONG_MAX, (live && cnt > 0) ? 1 : 0};
-  float vd[2] = {fe * Pe, Pe};
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    vi[0] += __shfl_xor_sync(0xffffffffu, vi[0], o);
-    vi[1] += __shfl_xor_sync(0xffffffffu, vi[1], o);
-    vi[2] = max(vi[2], __shfl_xor_sync(0xffffffffu, vi[2], o));
-    vi[3] = min(vi[3], __shfl_xor_sync(0xffffffffu, vi[3], o));
-    vi[4] += __shfl_xor_sync(0xffffffffu, vi[4], o);
-    vd[0] += __shfl_xor_sync(0xffffffffu, vd[0], o);
-    vd[1] += __shfl_xor_sync(0xffffffffu, vd[1], o);
-  }
+  for (int o = 16; o > 0; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
   if (lane == 0) {
-    for (int i = 0; i < 5; ++i) s_red_i[i][warp] = vi[i];
-    s_red_d[0][warp] = vd[0];
-    s_red_d[1][warp] = vd[1];
-  }
-  __syncthreads();
-  if (warp == 0) {
-    const int nw = blockDim.x >> 5;
-    long long a0 = lane < nw ? s_red_i[0][lane] : 0, a1 = lane < nw ? s_red_i[1][lane] : 0;
-    long long a2 = lane < nw ? s_red_i[2][lane] : LLONG_MIN, a3 = lane < nw ? s_red_i[3][lane] : LLONG_MAX;
-    long long a4 = lane < nw ? s_red_i[4][lane] : 0;
-    float d0 = lane < nw ? s_red_d[0][lane] : 0.f, d1 = lane < nw ? s_red_d[1][lane] : 0.f;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      a0 += __shfl_xor_sync(0xffffffffu, a0, o);
-      a1 += __shfl_xor_sync(0xffffffffu, a1, o);
-      a2 = max(a2, __shfl_xor_sync(0xffffffffu, a2, o));
-      a3 = min(a3, __shfl_xor_sync(0xffffffffu, a3, o));
-      a4 += __shfl_xor_sync(0xffffffffu, a4, o);
-      d0 += __shfl_xor_sync(0xffffffffu, d0, o);
-      d1 += __shfl_xor_sync(0xffffffffu, d1, o);
-    }
-    if (lane == 0) {
-      lrm_route_summary s;
-      s.N = static_cast<int32_t>(N);
-      s.C = static_cast<int32_t>(C);
-      s.slots = static_cast<int32_t>(C * E);
-      s.dropped = static_cast<int32_t>(a0);
-      s.retained = static_cast<int32_t>(a1);
-      s.max_count = static_cast<int32_t>(a2);
-      s.min_count = static_cast<int32_t>(a3);
-      s.nonempty = static_cast<int32_t>(a4);
-      s.aux_unscaled = static_cast<float>(E) * d0;
-      s.drop_rate = N > 0 ? static_cast<float>(a0) / static_cast<float>(N) : 0.f;
-      s.util = C > 0 ? static_cast<float>(N - a0) / static_cast<float>(C * E) : 0.f;
-      s.rho_real = N > 0 ? static_cast<float>(a1) / static_cast<float>(N) : 0.f;
-      s.max_over_mean = N > 0 ? static_cast<float>(a2) * static_cast<float>(E) / static_cast<float>(N) : 0.f;
-      s.sum_P = d1;
-      *summary = s;
-    }
+    const int cnt = run;
+    const long long C = (static_cast<long long>(cf_num) * N) / (static_cast<long long>(cf_den) * E);
+    const long long m = cnt < C ? cnt : C;
+    counts[x] = cnt;
+    // fp32 throughout: fp64 runs at a small fraction of the fp32 rate on this part
+    P[x] = T > 0 ? ps / static_cast<float>(T) : 0.f;
+    f[x] = N > 0 ? static_cast<float>(cnt) / static_cast<float>(N) : 0.f;
+    quota[x] = static_cast<int32_t>((static_cast<long long>(rho_num) * m + rho_den - 1) / rho_den);
   }
 }
 
+// The summary of the step from the per-expert outputs (one warp, a fixed
+// reduction order, so the floats are the same on every run).
+__device__ void write_summary(int T, int E, int k, int32_t cf_num, int32_t cf_den, const int32_t* __restrict__ counts,
+                              const float* __restrict__ P, const float* __restrict__ f,
+                              const int32_t* __restrict__ quota, lrm_route_summary* __restrict__ summary) {
+  const int lane = threadIdx.x & 31;
+  const long long N = static_cast<long long>(T) * k;
+  const long long C = (static_cast<long long>(cf_num) * N) / (static_cast<long long>(cf_den) * E);
+  long long drop = 0, ret = 0, mx = LLONG_MIN, mn = LLONG_MAX, nonempty = 0;
+  float fp = 0.f, sp = 0.f;
+  for (int e = lane; e < E; e += 32) {
+    const long long cnt = counts[e];
+    drop += cnt > C ? cnt - C : 0;
+    ret += quota[e];
+    mx = max(mx, cnt);
+    mn = min(mn, cnt);
+    nonempty += cnt > 0 ? 1 : 0;
+    fp += f[e] * P[e];
+    sp += P[e];
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    drop += __shfl_xor_sync(0xffffffffu, drop, o);
+    ret += __shfl_xor_sync(0xffffffffu, ret, o);
+    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    nonempty += __shfl_xor_sync(0xffffffffu, nonempty, o);
+    fp += __shfl_xor_sync(0xffffffffu, fp, o);
+    sp += __shfl_xor_sync(0xffffffffu, sp, o);
+  }
+  if (lane == 0) {
+    lrm_route_summary s;
+    s.N = static_cast<int32_t>(N);
+    s.C = static_cast<int32_t>(C);
+    s.slots = static_cast<int32_t>(C * E);
+    s.dropped = static_cast<int32_t>(drop);
+    s.retained = static_cast<int32_t>(ret);
+    s.max_count = static_cast<int32_t>(mx);
+    s.min_count = static_cast<int32_t>(mn);
+    s.nonempty = static_cast<int32_t>(nonempty);
+    s.aux_unscaled = static_cast<float>(E) * fp;
+    s.drop_rate = N > 0 ? static_cast<float>(drop) / static_cast<float>(N) : 0.f;
+    s.util = C > 0 ? static_cast<float>(N - drop) / static_cast<float>(C * E) : 0.f;
+    s.rho_real = N > 0 ? static_cast<float>(ret) / static_cast<float>(N) : 0.f;
+    s.max_over_mean = N > 0 ? static_cast<float>(mx) * static_cast<float>(E) / static_cast<float>(N) : 0.f;
+    s.sum_P = sp;
+    *summary = s;
+  }
+}
+
+// Expert offsets (exclusive scan of the counts) in every block; block 0 also
+// writes offsets[] and the summary.  Then the stable scatter of the block's
+// pairs (none when the layer has no token: one block is launched for the
+// offsets and the summary).
 __global__ void __launch_bounds__(RS_THREADS) rs_scatter(const int32_t* __restrict__ idx, int T, int E, int k,
-                                                         int tpb, int nblk, const int32_t* __restrict__ ws_base,
+                                                         int tpb, int nblk, int32_t cf_num, int32_t cf_den,
+                                                         const int32_t* __restrict__ ws_base,
+                                                         const int32_t* __restrict__ counts,
+                                                         const float* __restrict__ P, const float* __restrict__ f,
+                                                         const int32_t* __restrict__ quota,
+                                                         int32_t* __restrict__ offsets,
+                                                         lrm_route_summary* __restrict__ summary,
                                                          int32_t* __restrict__ bucket) {
   extern __shared__ int rs_cnt[];  // [RS_WARPS][E], then the staged ids
+  __shared__ int s_off[1024];      // first bucket slot of every expert (E <= 1024)
   int* s_ids = rs_cnt + RS_WARPS * E;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (warp == 0) {
+    // a run of experts per lane, then a warp scan
+    const int per = (E + 31) / 32;
+    const int e0 = lane * per;
+    int local = 0;
+    for (int e = e0; e < min(E, e0 + per); ++e) local += counts[e];
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    int run = incl - local;
+    for (int e = e0; e < min(E, e0 + per); ++e) {
+      s_off[e] = run;
+      if (blockIdx.x == 0) offsets[e] = run;
+      run += counts[e];
+    }
+    if (blockIdx.x == 0 && lane == 31) offsets[E] = incl;
+  } else if (warp == 1 && blockIdx.x == 0) {
+    write_summary(T, E, k, cf_num, cf_den, counts, P, f, quota, summary);
+  }
+  if (nblk == 0) return;
   for (int i = tid; i < RS_WARPS * E; i += RS_THREADS) rs_cnt[i] = 0;
   const int p0 = blockIdx.x * tpb * k;
   const int p1 = min(T, (blockIdx.x + 1) * tpb) * k;
@@ -330,7 +317,7 @@ __global__ void __launch_bounds__(RS_THREADS) rs_scatter(const int32_t* __restri
   __syncthreads();
   // per expert: the block's base offset, then exclusive prefix over the warps
   for (int e = tid; e < E; e += RS_THREADS) {
-    int run = ws_base[static_cast<size_t>(e) * nblk + blockIdx.x];
+    int run = s_off[e] + ws_base[static_cast<size_t>(e) * nblk + blockIdx.x];
 #pragma unroll
     for (int w = 0; w < RS_WARPS; ++w) {
       const int c = rs_cnt[w * E + e];
@@ -367,6 +354,46 @@ cudaError_t launch_count(int nblk, size_t smem, cudaStream_t s, const float* log
   return cudaGetLastError();
 }
 
+// The three launches of the step on `s` (shared by both entry points).
+lrm_status launch_route_stats(lrm_ctx* ctx, const RsLayout& L, const lrm_dims& dims, const float* logits,
+                              const int32_t* expert_idx, int32_t cf_num, int32_t cf_den, int32_t rho_num,
+                              int32_t rho_den, int32_t* counts, int32_t* offsets, int32_t* bucket, float* P, float* f,
+                              int32_t* quota, lrm_route_summary* summary, int32_t* ws_hist, float* ws_p,
+                              cudaStream_t s) {
+  if (L.nblk > 0) {
+    const size_t smem1 = (RS_WARPS * dims.E + dims.E + RS_PAIRS_PER_BLOCK) * sizeof(float);
+    const int vpl = (dims.E + 31) / 32;
+    cudaError_t e;
+    if (vpl <= 1)
+      e = launch_count<1>(L.nblk, smem1, s, logits, expert_idx, dims, L.tpb, ws_hist, ws_p, ctx->d_status);
+    else if (vpl <= 2)
+      e = launch_count<2>(L.nblk, smem1, s, logits, expert_idx, dims, L.tpb, ws_hist, ws_p, ctx->d_status);
+    else if (vpl <= 4)
+      e = launch_count<4>(L.nblk, smem1, s, logits, expert_idx, dims, L.tpb, ws_hist, ws_p, ctx->d_status);
+    else if (vpl <= 8)
+      e = launch_count<8>(L.nblk, smem1, s, logits, expert_idx, dims, L.tpb, ws_hist, ws_p, ctx->d_status);
+    else if (vpl <= 16)
+      e = launch_count<16>(L.nblk, smem1, s, logits, expert_idx, dims, L.tpb, ws_hist, ws_p, ctx->d_status);
+    else
+      e = launch_count<32>(L.nblk, smem1, s, logits, expert_idx, dims, L.tpb, ws_hist, ws_p, ctx->d_status);
+    if (e != cudaSuccess) return LRM_ERR_CUDA;
+  }
+  rs_rows<<<(dims.E + RR_WARPS - 1) / RR_WARPS, RR_THREADS, 0, s>>>(dims.T, dims.E, dims.k, L.nblk, cf_num, cf_den,
+                                                                     rho_num, rho_den, ws_hist, ws_p, counts, P, f,
+                                                                     quota);
+  lrm_status st = launch_status();
+  if (st != LRM_OK) return st;
+  const size_t smem3 = (RS_WARPS * dims.E + RS_PAIRS_PER_BLOCK) * sizeof(int);
+  if (smem3 > 48 * 1024 &&
+      cudaFuncSetAttribute(rs_scatter, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem3)) !=
+          cudaSuccess)
+    return LRM_ERR_CUDA;
+  rs_scatter<<<L.nblk > 0 ? L.nblk : 1, RS_THREADS, smem3, s>>>(expert_idx, dims.T, dims.E, dims.k, L.tpb, L.nblk,
+                                                                 cf_num, cf_den, ws_hist, counts, P, f, quota,
+                                                                 offsets, summary, bucket);
+  return launch_status();
+}
+
 }  // namespace
 
 size_t route_stats_workspace_bytes(const lrm_dims& d) { return rs_layout(d).bytes; }
@@ -401,38 +428,8 @@ extern "C" lrm_status lrm_route_stats(lrm_ctx* ctx, const float* logits, const i
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int32_t* ws_hist = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + L.hist_off);
   float* ws_p = reinterpret_cast<float*>(static_cast<char*>(ws) + L.p_off);
-  if (L.nblk > 0) {
-    const size_t smem1 = (RS_WARPS * dims.E + dims.E + RS_PAIRS_PER_BLOCK) * sizeof(float);
-    const int vpl = (dims.E + 31) / 32;
-    cudaError_t e;
-    if (vpl <= 1)
-      e = launch_count<1>(L.nblk, smem1, s, logits, expert_idx, dims, L.tpb, ws_hist, ws_p, ctx->d_status);
-    else if (vpl <= 2)
-      e = launch_count<2>(L.nblk, smem1, s, logits, expert_idx, dims, L.tpb, ws_hist, ws_p, ctx->d_status);
-    else if (vpl <= 4)
-      e = launch_count<4>(L.nblk, smem1, s, logits, expert_idx, dims, L.tpb, ws_hist, ws_p, ctx->d_status);
-    else if (vpl <= 8)
-      e = launch_count<8>(L.nblk, smem1, s, logits, expert_idx, dims, L.tpb, ws_hist, ws_p, ctx->d_status);
-    else if (vpl <= 16)
-      e = launch_count<16>(L.nblk, smem1, s, logits, expert_idx, dims, L.tpb, ws_hist, ws_p, ctx->d_status);
-    else
-      e = launch_count<32>(L.nblk, smem1, s, logits, expert_idx, dims, L.tpb, ws_hist, ws_p, ctx->d_status);
-    if (e != cudaSuccess) return LRM_ERR_CUDA;
-  }
-  rs_finalize<<<1, RS_FIN_THREADS, 0, s>>>(dims.T, dims.E, dims.k, L.nblk, cf_num, cf_den, rho_num, rho_den,
-                                           ws_hist, ws_p, counts, offsets, P, f, quota, summary);
-  if ((st = launch_status()) != LRM_OK) return st;
-  if (L.nblk > 0) {
-    const size_t smem3 = (RS_WARPS * dims.E + RS_PAIRS_PER_BLOCK) * sizeof(int);
-    if (smem3 > 48 * 1024 &&
-        cudaFuncSetAttribute(rs_scatter, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem3)) !=
-            cudaSuccess)
-      return LRM_ERR_CUDA;
-    rs_scatter<<<L.nblk, RS_THREADS, smem3, s>>>(expert_idx, dims.T, dims.E, dims.k, L.tpb, L.nblk, ws_hist,
-                                                 bucket);
-    if ((st = launch_status()) != LRM_OK) return st;
-  }
-  return LRM_OK;
+  return launch_route_stats(ctx, L, dims, logits, expert_idx, cf_num, cf_den, rho_num, rho_den, counts, offsets,
+                            bucket, P, f, quota, summary, ws_hist, ws_p, s);
 }
 
 // ---------------------------------------------------------------------------
@@ -496,36 +493,6 @@ extern "C" lrm_status lrm_route_stats_noalloc(lrm_ctx* ctx, const float* logits,
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int32_t* ws_hist = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + L.hist_off);
   float* ws_p = reinterpret_cast<float*>(static_cast<char*>(ws) + L.p_off);
-  if (L.nblk > 0) {
-    const size_t smem1 = (RS_WARPS * dims.E + dims.E + RS_PAIRS_PER_BLOCK) * sizeof(float);
-    const int vpl = (dims.E + 31) / 32;
-    cudaError_t e;
-    if (vpl <= 1)
-      e = launch_count<1>(L.nblk, smem1, s, logits, expert_idx, dims, L.tpb, ws_hist, ws_p, ctx->d_status);
-    else if (vpl <= 2)
-      e = launch_count<2>(L.nblk, smem1, s, logits, expert_idx, dims, L.tpb, ws_hist, ws_p, ctx->d_status);
-    else if (vpl <= 4)
-      e = launch_count<4>(L.nblk, smem1, s, logits, expert_idx, dims, L.tpb, ws_hist, ws_p, ctx->d_status);
-    else if (vpl <= 8)
-      e = launch_count<8>(L.nblk, smem1, s, logits, expert_idx, dims, L.tpb, ws_hist, ws_p, ctx->d_status);
-    else if (vpl <= 16)
-      e = launch_count<16>(L.nblk, smem1, s, logits, expert_idx, dims, L.tpb, ws_hist, ws_p, ctx->d_status);
-    else
-      e = launch_count<32>(L.nblk, smem1, s, logits, expert_idx, dims, L.tpb, ws_hist, ws_p, ctx->d_status);
-    if (e != cudaSuccess) return LRM_ERR_CUDA;
-  }
-  rs_finalize<<<1, RS_FIN_THREADS, 0, s>>>(dims.T, dims.E, dims.k, L.nblk, cf_num, cf_den, rho_num, rho_den,
-                                           ws_hist, ws_p, counts, offsets, P, f, quota, summary);
-  if ((st = launch_status()) != LRM_OK) return st;
-  if (L.nblk > 0) {
-    const size_t smem3 = (RS_WARPS * dims.E + RS_PAIRS_PER_BLOCK) * sizeof(int);
-    if (smem3 > 48 * 1024 &&
-        cudaFuncSetAttribute(rs_scatter, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem3)) !=
-            cudaSuccess)
-      return LRM_ERR_CUDA;
-    rs_scatter<<<L.nblk, RS_THREADS, smem3, s>>>(expert_idx, dims.T, dims.E, dims.k, L.tpb, L.nblk, ws_hist,
-                                                 bucket);
-    if ((st = launch_status()) != LRM_OK) return st;
-  }
-  return LRM_OK;
+  return launch_route_stats(ctx, L, dims, logits, expert_idx, cf_num, cf_den, rho_num, rho_den, counts, offsets,
+                            bucket, P, f, quota, summary, ws_hist, ws_p, s);
 }
