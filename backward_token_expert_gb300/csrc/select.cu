@@ -42,6 +42,55 @@ constexpr int SEL_SAMPLE_MIN = 4096; // experts with more candidates bracket the
 
 __device__ __forceinline__ uint32_t score_key(float r) { return __float_as_uint(r) & 0x7FFFFFFFu; }
 
+// Exclusive prefix of per-warp totals (vals[w] for w < SEL_WARPS) at this
+// thread's warp, and their sum; every warp scans the 32 totals itself.
+__device__ __forceinline__ int warp_totals_prefix(const int* vals, int warp, int lane, int* total) {
+  const int v = vals[lane];
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  *total = __shfl_sync(0xffffffffu, incl, 31);
+  return __shfl_sync(0xffffffffu, incl - v, warp);
+}
+
+// Contiguous candidate range [w0, w1) of warp `warp` over n keys, a multiple
+// of 32 wide, so that compaction keeps ascending order within a warp.
+__device__ __forceinline__ void warp_range(int n, int warp, int& w0, int& w1) {
+  const int span = ((n + SEL_WARPS - 1) / SEL_WARPS + 31) & ~31;
+  w0 = min(n, warp * span);
+  w1 = min(n, w0 + span);
+}
+
+// Writes the keys of src[0, n) that satisfy pred into dst without atomics:
+// each warp counts its contiguous range, the warp totals are scanned, then
+// each warp writes its matches from its base.  Returns the number written.
+template <typename Pred>
+__device__ __forceinline__ int compact_keys(const uint32_t* src, int n, uint32_t* dst, int* s_cnt, Pred pred) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  int w0, w1;
+  warp_range(n, warp, w0, w1);
+  int c = 0;
+#pragma unroll 4
+  for (int i = w0 + lane; i - lane < w1; i += 32) c += __popc(__ballot_sync(0xffffffffu, i < w1 && pred(src[i])));
+  if (lane == 0) s_cnt[warp] = c;
+  __syncthreads();
+  int total;
+  int base = warp_totals_prefix(s_cnt, warp, lane, &total);
+  for (int i = w0 + lane; i - lane < w1; i += 32) {
+    const uint32_t k = i < w1 ? src[i] : 0u;
+    const bool m = i < w1 && pred(k);
+    const unsigned bal = __ballot_sync(0xffffffffu, m);
+    if (m) dst[base + __popc(bal & lt_mask)] = k;
+    base += __popc(bal);
+  }
+  __syncthreads();
+  return total;
+}
+
 __global__ void __launch_bounds__(GATHER_THREADS) select_gather_kernel(const float* __restrict__ R,
                                                                        const int32_t* __restrict__ bucket, int N,
                                                                        uint32_t* __restrict__ keys) {
@@ -74,7 +123,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
   __shared__ int s_hist[SEL_MAX_BINS];
   __shared__ int s_warp[SEL_WARPS];
   __shared__ int s_wgt[SEL_WARPS], s_weq[SEL_WARPS];
-  __shared__ int s_total, s_ncand;
+  __shared__ int s_total;
   __shared__ int s_digit, s_above, s_bincnt;
 
   const int e = blockIdx.x;
@@ -147,40 +196,45 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
     // the sample keys a few standard deviations either side of the expected
     // rank of the boundary, count the keys above and inside that bracket with
     // ballots, and if the boundary lies inside, keep only the bracket's keys.
+    // bitonic sort, one key per thread: exchanges with a partner in the same
+    // warp (j < 32) go through shuffles, the others through shared memory
     uint32_t* samp = reinterpret_cast<uint32_t*>(s_hist);
-    samp[tid] = K[static_cast<int>((static_cast<long long>(tid) * n) / SEL_THREADS)];
-    __syncthreads();
+    uint32_t mine = K[static_cast<int>((static_cast<long long>(tid) * n) / SEL_THREADS)];
     for (int kk = 2; kk <= SEL_THREADS; kk <<= 1) {
       for (int j = kk >> 1; j > 0; j >>= 1) {
-        const int ixj = tid ^ j;
-        if (ixj > tid) {
-          const uint32_t a = samp[tid], b = samp[ixj];
-          if (((tid & kk) == 0) ? (a < b) : (a > b)) {
-            samp[tid] = b;
-            samp[ixj] = a;
-          }
+        uint32_t other;
+        if (j >= 32) {
+          samp[tid] = mine;
+          __syncthreads();
+          other = samp[tid ^ j];
+          __syncthreads();
+        } else {
+          other = __shfl_xor_sync(0xffffffffu, mine, j);
         }
-        __syncthreads();
+        // descending overall: the lower index of a pair keeps the larger key
+        // in blocks with (tid & kk) == 0, the smaller one otherwise
+        const bool lower = (tid & j) == 0;
+        const bool desc = (tid & kk) == 0;
+        mine = (lower == desc) ? max(mine, other) : min(mine, other);
       }
     }
+    samp[tid] = mine;
+    __syncthreads();
     const float pr = static_cast<float>(q) / static_cast<float>(n);
     const int r = min(SEL_THREADS - 1, static_cast<int>((static_cast<long long>(q) * SEL_THREADS) / n));
     const int d = static_cast<int>(3.f * sqrtf(SEL_THREADS * pr * (1.f - pr))) + 8;
     const uint32_t hi = samp[max(0, r - d)];
     const uint32_t lo = samp[min(SEL_THREADS - 1, r + d)];
     int c_gt = 0, c_in = 0;
-    for (int i0 = 0; i0 < n; i0 += SEL_THREADS * SEL_GATHER) {
-      uint32_t kk[SEL_GATHER];
-#pragma unroll
-      for (int j = 0; j < SEL_GATHER; ++j) {
-        const int i = i0 + j * SEL_THREADS + tid;
-        kk[j] = i < n ? K[i] : 0u;
-      }
-#pragma unroll
-      for (int j = 0; j < SEL_GATHER; ++j) {
-        const bool live = i0 + j * SEL_THREADS + tid < n;
-        c_gt += __popc(__ballot_sync(0xffffffffu, live && kk[j] > hi));
-        c_in += __popc(__ballot_sync(0xffffffffu, live && kk[j] >= lo && kk[j] <= hi));
+    {
+      int w0, w1;
+      warp_range(n, warp, w0, w1);
+#pragma unroll 4
+      for (int i = w0 + lane; i - lane < w1; i += 32) {
+        const bool live = i < w1;
+        const uint32_t kk = live ? K[i] : 0u;
+        c_gt += __popc(__ballot_sync(0xffffffffu, live && kk > hi));
+        c_in += __popc(__ballot_sync(0xffffffffu, live && kk >= lo && kk <= hi));
       }
     }
     if (lane == 0) {
@@ -188,26 +242,11 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
       s_weq[warp] = c_in;
     }
     __syncthreads();
-    c_gt = 0;
-    c_in = 0;
-    for (int w = 0; w < SEL_WARPS; ++w) {
-      c_gt += s_wgt[w];
-      c_in += s_weq[w];
-    }
+    warp_totals_prefix(s_wgt, warp, lane, &c_gt);
+    warp_totals_prefix(s_weq, warp, lane, &c_in);
     if (c_gt < q && q <= c_gt + c_in && c_in <= SEL_CAND_KEYS) {
-      if (tid == 0) s_ncand = 0;
-      __syncthreads();
-      for (int i0 = 0; i0 < n; i0 += SEL_THREADS) {
-        const int i = i0 + tid;
-        const uint32_t kk = i < n ? K[i] : 0u;
-        const bool m = i < n && kk >= lo && kk <= hi;
-        const unsigned bal = __ballot_sync(0xffffffffu, m);
-        int wbase = 0;
-        if (lane == 0 && bal != 0u) wbase = atomicAdd(&s_ncand, __popc(bal));
-        wbase = __shfl_sync(0xffffffffu, wbase, 0);
-        if (m) s_cand[wbase + __popc(bal & lt_mask)] = kk;
-      }
-      __syncthreads();
+      __syncthreads();  // every warp has read the totals
+      compact_keys(K, n, s_cand, s_wgt, [lo, hi](uint32_t kk) { return kk >= lo && kk <= hi; });
       C = s_cand;
       nc = c_in;
       want = q - c_gt;
@@ -274,21 +313,8 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
       if (lo_bit == 0) break;
       // once the boundary bin fits, later passes scan only its keys
       if (C == K && bincnt <= SEL_CAND_KEYS) {
-        if (tid == 0) s_ncand = 0;
-        __syncthreads();
-        for (int i0 = 0; i0 < nc; i0 += SEL_THREADS) {
-          const int i = i0 + tid;
-          const uint32_t kk = i < nc ? C[i] : 0u;
-          const bool m = i < nc && (kk & mask) == prefix;
-          const unsigned bal = __ballot_sync(0xffffffffu, m);
-          int wbase = 0;
-          if (lane == 0 && bal != 0u) wbase = atomicAdd(&s_ncand, __popc(bal));
-          wbase = __shfl_sync(0xffffffffu, wbase, 0);
-          if (m) s_cand[wbase + __popc(bal & lt_mask)] = kk;
-        }
-        __syncthreads();
+        nc = compact_keys(C, nc, s_cand, s_wgt, [mask, prefix](uint32_t kk) { return (kk & mask) == prefix; });
         C = s_cand;
-        nc = s_ncand;
       }
     }
   }
@@ -298,8 +324,8 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
   // Count its kept keys, scan the 32 warp totals, then place the kept ids:
   // key x goes to (#keys above tau before x) + min(#keys equal to tau before
   // x, want), keeping the first `want` keys equal to tau.
-  const int span = ((n + SEL_WARPS - 1) / SEL_WARPS + 31) & ~31;
-  const int w0 = min(n, warp * span), w1 = min(n, w0 + span);
+  int w0, w1;
+  warp_range(n, warp, w0, w1);
   int cg = 0, ce = 0;
   for (int i0 = w0; i0 < w1; i0 += 32 * SEL_OUT_UNROLL) {
     uint32_t kk[SEL_OUT_UNROLL];
@@ -320,11 +346,9 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
     s_weq[warp] = ce;
   }
   __syncthreads();
-  int gtb = 0, eqb = 0;
-  for (int w = 0; w < warp; ++w) {
-    gtb += s_wgt[w];
-    eqb += s_weq[w];
-  }
+  int tot_unused;
+  int gtb = warp_totals_prefix(s_wgt, warp, lane, &tot_unused);
+  int eqb = warp_totals_prefix(s_weq, warp, lane, &tot_unused);
   for (int i0 = w0; i0 < w1; i0 += 32 * SEL_OUT_UNROLL) {
     uint32_t kk[SEL_OUT_UNROLL];
     int id[SEL_OUT_UNROLL];
