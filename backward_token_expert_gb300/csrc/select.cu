@@ -36,7 +36,9 @@ constexpr int SEL_SMEM_KEYS = 40960;
 constexpr int SEL_GATHER = 4;  // independent loads in flight per thread
 constexpr int SEL_MAX_BINS = 2048;
 constexpr int GATHER_THREADS = 256;
-constexpr int SEL_CAND_KEYS = 8192;  // shared-memory room for the boundary bin's keys
+constexpr int SEL_CAND_KEYS = 8192;  // shared-memory room for candidate keys
+constexpr int SEL_REGION = SEL_CAND_KEYS / SEL_WARPS;  // candidate keys a warp may keep
+constexpr int SEL_LOAD = 8;                             // keys per thread in flight while loading an expert
 constexpr int SEL_OUT_UNROLL = 16;   // 32-candidate steps whose loads are issued together
 constexpr int SEL_SAMPLE_MIN = 4096; // experts with more candidates bracket the boundary by sampling
 
@@ -64,33 +66,6 @@ __device__ __forceinline__ void warp_range(int n, int warp, int& w0, int& w1) {
   w1 = min(n, w0 + span);
 }
 
-// Writes the keys of src[0, n) that satisfy pred into dst without atomics:
-// each warp counts its contiguous range, the warp totals are scanned, then
-// each warp writes its matches from its base.  Returns the number written.
-template <typename Pred>
-__device__ __forceinline__ int compact_keys(const uint32_t* src, int n, uint32_t* dst, int* s_cnt, Pred pred) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const unsigned lt_mask = (1u << lane) - 1u;
-  int w0, w1;
-  warp_range(n, warp, w0, w1);
-  int c = 0;
-#pragma unroll 4
-  for (int i = w0 + lane; i - lane < w1; i += 32) c += __popc(__ballot_sync(0xffffffffu, i < w1 && pred(src[i])));
-  if (lane == 0) s_cnt[warp] = c;
-  __syncthreads();
-  int total;
-  int base = warp_totals_prefix(s_cnt, warp, lane, &total);
-  for (int i = w0 + lane; i - lane < w1; i += 32) {
-    const uint32_t k = i < w1 ? src[i] : 0u;
-    const bool m = i < w1 && pred(k);
-    const unsigned bal = __ballot_sync(0xffffffffu, m);
-    if (m) dst[base + __popc(bal & lt_mask)] = k;
-    base += __popc(bal);
-  }
-  __syncthreads();
-  return total;
-}
-
 __global__ void __launch_bounds__(GATHER_THREADS) select_gather_kernel(const float* __restrict__ R,
                                                                        const int32_t* __restrict__ bucket, int N,
                                                                        uint32_t* __restrict__ keys) {
@@ -114,12 +89,11 @@ __global__ void __launch_bounds__(GATHER_THREADS) select_gather_kernel(const flo
 }
 
 __global__ void __launch_bounds__(SEL_THREADS, 1)
-    select_kernel(const float* __restrict__ R, const int32_t* __restrict__ offsets,
-                  const int32_t* __restrict__ bucket, const int32_t* __restrict__ quota, int E, int max_rows,
-                  int32_t* __restrict__ sel_offsets, int32_t* __restrict__ sel_ids,
-                  const uint32_t* __restrict__ keys_ws, unsigned int* status) {
+    select_kernel(const int32_t* __restrict__ offsets, const int32_t* __restrict__ bucket,
+                  const int32_t* __restrict__ quota, int E, int max_rows, int32_t* __restrict__ sel_offsets,
+                  int32_t* __restrict__ sel_ids, const uint32_t* __restrict__ keys_ws, unsigned int* status) {
   extern __shared__ uint32_t s_keys[];
-  uint32_t* s_cand = s_keys + SEL_SMEM_KEYS;  // [SEL_CAND_KEYS] keys of the boundary bin
+  uint32_t* s_cand = s_keys + SEL_SMEM_KEYS;  // SEL_WARPS regions of SEL_REGION candidate keys
   __shared__ int s_hist[SEL_MAX_BINS];
   __shared__ int s_warp[SEL_WARPS];
   __shared__ int s_wgt[SEL_WARPS], s_weq[SEL_WARPS];
@@ -141,7 +115,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
   if (lane == 0) s_warp[warp] = part;
   __syncthreads();
   int base = 0;
-#pragma unroll 8
+#pragma unroll
   for (int w = 0; w < SEL_WARPS; ++w) base += s_warp[w];
 
   const int off = __ldg(offsets + e);
@@ -168,15 +142,15 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
 
   const uint32_t* K = keys_ws + off;
   if (n <= SEL_SMEM_KEYS) {
-    for (int i0 = 0; i0 < n; i0 += SEL_THREADS * SEL_GATHER) {
-      uint32_t v[SEL_GATHER];
+    for (int i0 = 0; i0 < n; i0 += SEL_THREADS * SEL_LOAD) {
+      uint32_t v[SEL_LOAD];
 #pragma unroll
-      for (int j = 0; j < SEL_GATHER; ++j) {
+      for (int j = 0; j < SEL_LOAD; ++j) {
         const int i = i0 + j * SEL_THREADS + tid;
         v[j] = i < n ? __ldg(K + i) : 0u;
       }
 #pragma unroll
-      for (int j = 0; j < SEL_GATHER; ++j) {
+      for (int j = 0; j < SEL_LOAD; ++j) {
         const int i = i0 + j * SEL_THREADS + tid;
         if (i < n) s_keys[i] = v[j];
       }
@@ -185,29 +159,36 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
   }
   __syncthreads();
 
+  // Every pass below works on this warp's contiguous range [w0, w1) of the
+  // candidates (ascending u), and candidate keys it keeps go to its own
+  // region of s_cand, so no pass needs atomics or a block-wide compaction.
+  int w0, w1;
+  warp_range(n, warp, w0, w1);
+  uint32_t* region = s_cand + warp * SEL_REGION;
+
   uint32_t prefix = 0, mask = 0;
-  int want = q;           // keys still to take from C
+  int want = q;  // keys still to take among the radix candidates
   bool ge_mode = false;
-  uint32_t ge_floor = 0;  // in "key >= prefix" mode, keys below ge_floor are not candidates
-  const uint32_t* C = K;  // keys the next radix pass scans
-  int nc = n;
+  uint32_t ge_floor = 0;    // in "key >= prefix" mode, keys below ge_floor are not candidates
+  bool bracketed = false;   // the radix candidates are the sample bracket's keys
+  int w_gt_hi = 0, w_in = 0;  // this warp's keys above / inside the bracket
   if (n > SEL_SAMPLE_MIN) {
     // Sample select: sort 1024 evenly spaced keys (descending, bitonic), take
     // the sample keys a few standard deviations either side of the expected
-    // rank of the boundary, count the keys above and inside that bracket with
-    // ballots, and if the boundary lies inside, keep only the bracket's keys.
-    // bitonic sort, one key per thread: exchanges with a partner in the same
-    // warp (j < 32) go through shuffles, the others through shared memory
-    uint32_t* samp = reinterpret_cast<uint32_t*>(s_hist);
+    // rank of the boundary as a bracket [lo, hi].  One pass counts the keys
+    // above it and captures the keys inside it; when the boundary lies
+    // inside, only those keys go on to the radix select.
     uint32_t mine = K[static_cast<int>((static_cast<long long>(tid) * n) / SEL_THREADS)];
+    int sm_stage = 0;  // exchanges through shared memory alternate between two buffers
     for (int kk = 2; kk <= SEL_THREADS; kk <<= 1) {
       for (int j = kk >> 1; j > 0; j >>= 1) {
         uint32_t other;
         if (j >= 32) {
-          samp[tid] = mine;
+          uint32_t* buf = reinterpret_cast<uint32_t*>(s_hist) + (sm_stage & 1) * SEL_THREADS;
+          ++sm_stage;
+          buf[tid] = mine;
           __syncthreads();
-          other = samp[tid ^ j];
-          __syncthreads();
+          other = buf[tid ^ j];
         } else {
           other = __shfl_xor_sync(0xffffffffu, mine, j);
         }
@@ -218,6 +199,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
         mine = (lower == desc) ? max(mine, other) : min(mine, other);
       }
     }
+    uint32_t* samp = reinterpret_cast<uint32_t*>(s_hist) + (sm_stage & 1) * SEL_THREADS;
     samp[tid] = mine;
     __syncthreads();
     const float pr = static_cast<float>(q) / static_cast<float>(n);
@@ -225,39 +207,41 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
     const int d = static_cast<int>(3.f * sqrtf(SEL_THREADS * pr * (1.f - pr))) + 8;
     const uint32_t hi = samp[max(0, r - d)];
     const uint32_t lo = samp[min(SEL_THREADS - 1, r + d)];
-    int c_gt = 0, c_in = 0;
-    {
-      int w0, w1;
-      warp_range(n, warp, w0, w1);
 #pragma unroll 4
-      for (int i = w0 + lane; i - lane < w1; i += 32) {
-        const bool live = i < w1;
-        const uint32_t kk = live ? K[i] : 0u;
-        c_gt += __popc(__ballot_sync(0xffffffffu, live && kk > hi));
-        c_in += __popc(__ballot_sync(0xffffffffu, live && kk >= lo && kk <= hi));
-      }
+    for (int i = w0 + lane; i - lane < w1; i += 32) {
+      const bool live = i < w1;
+      const uint32_t kk = live ? K[i] : 0u;
+      w_gt_hi += __popc(__ballot_sync(0xffffffffu, live && kk > hi));
+      const bool in = live && kk >= lo && kk <= hi;
+      const unsigned bin = __ballot_sync(0xffffffffu, in);
+      const int pos = w_in + __popc(bin & lt_mask);
+      if (in && pos < SEL_REGION) region[pos] = kk;
+      w_in += __popc(bin);
     }
     if (lane == 0) {
-      s_wgt[warp] = c_gt;
-      s_weq[warp] = c_in;
+      s_wgt[warp] = w_gt_hi;
+      s_weq[warp] = w_in;
     }
     __syncthreads();
+    int c_gt, c_in;
     warp_totals_prefix(s_wgt, warp, lane, &c_gt);
     warp_totals_prefix(s_weq, warp, lane, &c_in);
-    if (c_gt < q && q <= c_gt + c_in && c_in <= SEL_CAND_KEYS) {
-      __syncthreads();  // every warp has read the totals
-      compact_keys(K, n, s_cand, s_wgt, [lo, hi](uint32_t kk) { return kk >= lo && kk <= hi; });
-      C = s_cand;
-      nc = c_in;
+    const int max_in = __reduce_max_sync(0xffffffffu, s_weq[lane]);
+    if (c_gt < q && q <= c_gt + c_in && max_in <= SEL_REGION) {
+      bracketed = true;
       want = q - c_gt;
       ge_floor = lo;
     }
-    __syncthreads();  // the sample buffer is the histogram below
+    __syncthreads();  // the sample buffers are the histogram below
   }
-  // radix select of the want-th largest key of C: digits of at most 11 bits
+
+  // radix select of the want-th largest candidate: digits of at most 11 bits
   // from the top; the first one (bits 21-31) sees the sign-free exponent and
-  // the leading mantissa bits, where keys bunch into few bins and the
-  // warp-aggregated atomics stay cheap
+  // the leading mantissa bits.  Each warp histograms its own candidates: its
+  // region, or its whole range until the boundary bin fits in the regions.
+  const uint32_t* cand = bracketed ? region : K + w0;
+  int ncand = bracketed ? w_in : w1 - w0;
+  bool in_regions = bracketed;
   {
     int lo_bit = 32;  // bits [lo_bit, 32) of the boundary key are known
     while (lo_bit > 0) {
@@ -267,35 +251,27 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
       const uint32_t dmask = static_cast<uint32_t>(nbins - 1);
       for (int b = tid; b < nbins; b += SEL_THREADS) s_hist[b] = 0;
       __syncthreads();
-      for (int i0 = 0; i0 < nc; i0 += SEL_THREADS * SEL_GATHER) {
-        uint32_t kk[SEL_GATHER];
-#pragma unroll
-        for (int j = 0; j < SEL_GATHER; ++j) {
-          const int i = i0 + j * SEL_THREADS + tid;
-          kk[j] = i < nc ? C[i] : 0u;
-        }
-#pragma unroll
-        for (int j = 0; j < SEL_GATHER; ++j) {
-          const int i = i0 + j * SEL_THREADS + tid;
-          int bin = SEL_MAX_BINS;
-          if (i < nc && (kk[j] & mask) == prefix) bin = static_cast<int>((kk[j] >> shift) & dmask);
-          const unsigned peers = __match_any_sync(0xffffffffu, bin);
-          if (bin < SEL_MAX_BINS && (peers & lt_mask) == 0) atomicAdd(&s_hist[bin], __popc(peers));
-        }
+#pragma unroll 4
+      for (int i = lane; i - lane < ncand; i += 32) {
+        const uint32_t kk = i < ncand ? cand[i] : 0u;
+        int bin = SEL_MAX_BINS;
+        if (i < ncand && (kk & mask) == prefix) bin = static_cast<int>((kk >> shift) & dmask);
+        const unsigned peers = __match_any_sync(0xffffffffu, bin);
+        if (bin < SEL_MAX_BINS && (peers & lt_mask) == 0) atomicAdd(&s_hist[bin], __popc(peers));
       }
       __syncthreads();
       // thread t owns bins hi = nbins-1-2t and hi-1 (descending); "above" counts
       // every key of the current prefix in a higher bin
-      const int hi = nbins - 1 - 2 * tid;
-      const int c_hi = hi >= 0 ? s_hist[hi] : 0;
-      const int c_lo = hi >= 1 ? s_hist[hi - 1] : 0;
+      const int hb = nbins - 1 - 2 * tid;
+      const int c_hi = hb >= 0 ? s_hist[hb] : 0;
+      const int c_lo = hb >= 1 ? s_hist[hb - 1] : 0;
       const int above = block_exclusive_scan_1024(c_hi + c_lo, s_warp, &s_total);
-      if (hi >= 0 && above < want && want <= above + c_hi) {
-        s_digit = hi;
+      if (hb >= 0 && above < want && want <= above + c_hi) {
+        s_digit = hb;
         s_above = above;
         s_bincnt = c_hi;
-      } else if (hi >= 1 && above + c_hi < want && want <= above + c_hi + c_lo) {
-        s_digit = hi - 1;
+      } else if (hb >= 1 && above + c_hi < want && want <= above + c_hi + c_lo) {
+        s_digit = hb - 1;
         s_above = above + c_hi;
         s_bincnt = c_lo;
       }
@@ -311,35 +287,43 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
         break;
       }
       if (lo_bit == 0) break;
-      // once the boundary bin fits, later passes scan only its keys
-      if (C == K && bincnt <= SEL_CAND_KEYS) {
-        nc = compact_keys(C, nc, s_cand, s_wgt, [mask, prefix](uint32_t kk) { return (kk & mask) == prefix; });
-        C = s_cand;
+      // once the boundary bin is small, each warp keeps only its keys of it
+      if (!in_regions && bincnt <= SEL_CAND_KEYS) {
+        int c = 0;
+#pragma unroll 4
+        for (int i = lane; i - lane < ncand; i += 32) {
+          const uint32_t kk = i < ncand ? cand[i] : 0u;
+          const bool m = i < ncand && (kk & mask) == prefix;
+          const unsigned bm = __ballot_sync(0xffffffffu, m);
+          const int pos = c + __popc(bm & lt_mask);
+          if (m && pos < SEL_REGION) region[pos] = kk;
+          c += __popc(bm);
+        }
+        if (!__syncthreads_or(c > SEL_REGION)) {
+          cand = region;
+          ncand = c;
+          in_regions = true;
+        }
       }
     }
   }
   const uint32_t tau = ge_mode ? max(prefix, ge_floor) : prefix;
 
-  // Output: each warp owns a contiguous range of the candidates (ascending u).
-  // Count its kept keys, scan the 32 warp totals, then place the kept ids:
-  // key x goes to (#keys above tau before x) + min(#keys equal to tau before
-  // x, want), keeping the first `want` keys equal to tau.
-  int w0, w1;
-  warp_range(n, warp, w0, w1);
+  // Output: count this warp's kept keys (keys above the bracket are kept; the
+  // rest are in its region, else scan the whole range), scan the 32 warp
+  // totals, then place the kept ids in ascending u: key x goes to (#keys above
+  // tau before x) + min(#keys equal to tau before x, want), keeping the first
+  // `want` keys equal to tau.
   int cg = 0, ce = 0;
-  for (int i0 = w0; i0 < w1; i0 += 32 * SEL_OUT_UNROLL) {
-    uint32_t kk[SEL_OUT_UNROLL];
-#pragma unroll
-    for (int j = 0; j < SEL_OUT_UNROLL; ++j) {
-      const int i = i0 + 32 * j + lane;
-      kk[j] = i < w1 ? K[i] : 0u;
-    }
-#pragma unroll
-    for (int j = 0; j < SEL_OUT_UNROLL; ++j) {
-      const bool live = i0 + 32 * j + lane < w1;
-      cg += __popc(__ballot_sync(0xffffffffu, live && (ge_mode ? (kk[j] >= tau) : (kk[j] > tau))));
-      ce += __popc(__ballot_sync(0xffffffffu, live && !ge_mode && kk[j] == tau));
-    }
+  const uint32_t* cnt_src = bracketed ? region : K + w0;
+  const int cnt_n = bracketed ? w_in : w1 - w0;
+  if (bracketed) cg = w_gt_hi;
+#pragma unroll 4
+  for (int i = lane; i - lane < cnt_n; i += 32) {
+    const bool live = i < cnt_n;
+    const uint32_t kk = live ? cnt_src[i] : 0u;
+    cg += __popc(__ballot_sync(0xffffffffu, live && (ge_mode ? (kk >= tau) : (kk > tau))));
+    ce += __popc(__ballot_sync(0xffffffffu, live && !ge_mode && kk == tau));
   }
   if (lane == 0) {
     s_wgt[warp] = cg;
@@ -419,7 +403,7 @@ extern "C" lrm_status lrm_select(lrm_ctx* ctx, const float* score, const int32_t
         score, bucket, N, static_cast<uint32_t*>(ws));
     if ((st = launch_status()) != LRM_OK) return st;
   }
-  select_kernel<<<dims.E, SEL_THREADS, smem, s>>>(score, offsets, bucket, quota, dims.E, max_rows, sel_offsets,
-                                                  sel_ids, static_cast<const uint32_t*>(ws), ctx->d_status);
+  select_kernel<<<dims.E, SEL_THREADS, smem, s>>>(offsets, bucket, quota, dims.E, max_rows, sel_offsets, sel_ids,
+                                                  static_cast<const uint32_t*>(ws), ctx->d_status);
   return launch_status();
 }
