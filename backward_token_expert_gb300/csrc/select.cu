@@ -36,8 +36,8 @@ constexpr int SEL_SMEM_KEYS = 40960;
 constexpr int SEL_GATHER = 4;  // independent loads in flight per thread
 constexpr int SEL_MAX_BINS = 2048;
 constexpr int GATHER_THREADS = 256;
-constexpr int SEL_CAND_KEYS = 8192;  // shared-memory room for candidate keys
-constexpr int SEL_REGION = SEL_CAND_KEYS / SEL_WARPS;  // candidate keys a warp may keep
+constexpr int SEL_REGION = 192;                         // candidate keys (and positions) a warp may keep
+constexpr int SEL_CAND_KEYS = SEL_REGION * SEL_WARPS;
 constexpr int SEL_LOAD = 8;                             // keys per thread in flight while loading an expert
 constexpr int SEL_OUT_UNROLL = 16;   // 32-candidate steps whose loads are issued together
 constexpr int SEL_SAMPLE_MIN = 4096; // experts with more candidates bracket the boundary by sampling
@@ -93,7 +93,8 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
                   const int32_t* __restrict__ quota, int E, int max_rows, int32_t* __restrict__ sel_offsets,
                   int32_t* __restrict__ sel_ids, const uint32_t* __restrict__ keys_ws, unsigned int* status) {
   extern __shared__ uint32_t s_keys[];
-  uint32_t* s_cand = s_keys + SEL_SMEM_KEYS;  // SEL_WARPS regions of SEL_REGION candidate keys
+  uint32_t* s_cand = s_keys + SEL_SMEM_KEYS;                           // SEL_WARPS regions of keys
+  uint16_t* s_cpos = reinterpret_cast<uint16_t*>(s_cand + SEL_CAND_KEYS);  // their positions in the warp's range
   __shared__ int s_hist[SEL_MAX_BINS];
   __shared__ int s_warp[SEL_WARPS];
   __shared__ int s_wgt[SEL_WARPS], s_weq[SEL_WARPS];
@@ -165,19 +166,23 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
   int w0, w1;
   warp_range(n, warp, w0, w1);
   uint32_t* region = s_cand + warp * SEL_REGION;
+  uint16_t* region_pos = s_cpos + warp * SEL_REGION;
 
   uint32_t prefix = 0, mask = 0;
   int want = q;  // keys still to take among the radix candidates
   bool ge_mode = false;
   uint32_t ge_floor = 0;    // in "key >= prefix" mode, keys below ge_floor are not candidates
   bool bracketed = false;   // the radix candidates are the sample bracket's keys
-  int w_gt_hi = 0, w_in = 0;  // this warp's keys above / inside the bracket
+  uint32_t cand_hi = 0xFFFFFFFFu;  // keys above this are kept without being radix candidates
+  int w_cap = 0;            // this warp's captured keys (at or above the bracket's low key)
   if (n > SEL_SAMPLE_MIN) {
     // Sample select: sort 1024 evenly spaced keys (descending, bitonic), take
     // the sample keys a few standard deviations either side of the expected
     // rank of the boundary as a bracket [lo, hi].  One pass counts the keys
-    // above it and captures the keys inside it; when the boundary lies
-    // inside, only those keys go on to the radix select.
+    // above and inside it and captures every key >= lo with its position, in
+    // order, into the warp's region; when the boundary lies inside the
+    // bracket, the bracket's keys go on to the radix select and the output
+    // reads only the regions.
     uint32_t mine = K[static_cast<int>((static_cast<long long>(tid) * n) / SEL_THREADS)];
     int sm_stage = 0;  // exchanges through shared memory alternate between two buffers
     for (int kk = 2; kk <= SEL_THREADS; kk <<= 1) {
@@ -207,30 +212,35 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
     const int d = static_cast<int>(3.f * sqrtf(SEL_THREADS * pr * (1.f - pr))) + 8;
     const uint32_t hi = samp[max(0, r - d)];
     const uint32_t lo = samp[min(SEL_THREADS - 1, r + d)];
+    int w_gt = 0;
 #pragma unroll 4
     for (int i = w0 + lane; i - lane < w1; i += 32) {
       const bool live = i < w1;
       const uint32_t kk = live ? K[i] : 0u;
-      w_gt_hi += __popc(__ballot_sync(0xffffffffu, live && kk > hi));
-      const bool in = live && kk >= lo && kk <= hi;
-      const unsigned bin = __ballot_sync(0xffffffffu, in);
-      const int pos = w_in + __popc(bin & lt_mask);
-      if (in && pos < SEL_REGION) region[pos] = kk;
-      w_in += __popc(bin);
+      w_gt += __popc(__ballot_sync(0xffffffffu, live && kk > hi));
+      const bool cap = live && kk >= lo;
+      const unsigned bc = __ballot_sync(0xffffffffu, cap);
+      const int pos = w_cap + __popc(bc & lt_mask);
+      if (cap && pos < SEL_REGION) {
+        region[pos] = kk;
+        region_pos[pos] = static_cast<uint16_t>(i - w0);
+      }
+      w_cap += __popc(bc);
     }
     if (lane == 0) {
-      s_wgt[warp] = w_gt_hi;
-      s_weq[warp] = w_in;
+      s_wgt[warp] = w_gt;
+      s_weq[warp] = w_cap;
     }
     __syncthreads();
-    int c_gt, c_in;
+    int c_gt, c_cap;
     warp_totals_prefix(s_wgt, warp, lane, &c_gt);
-    warp_totals_prefix(s_weq, warp, lane, &c_in);
-    const int max_in = __reduce_max_sync(0xffffffffu, s_weq[lane]);
-    if (c_gt < q && q <= c_gt + c_in && max_in <= SEL_REGION) {
+    warp_totals_prefix(s_weq, warp, lane, &c_cap);
+    const int max_cap = __reduce_max_sync(0xffffffffu, s_weq[lane]);
+    if (c_gt < q && q <= c_cap && max_cap <= SEL_REGION) {
       bracketed = true;
       want = q - c_gt;
       ge_floor = lo;
+      cand_hi = hi;
     }
     __syncthreads();  // the sample buffers are the histogram below
   }
@@ -240,7 +250,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
   // the leading mantissa bits.  Each warp histograms its own candidates: its
   // region, or its whole range until the boundary bin fits in the regions.
   const uint32_t* cand = bracketed ? region : K + w0;
-  int ncand = bracketed ? w_in : w1 - w0;
+  int ncand = bracketed ? w_cap : w1 - w0;
   bool in_regions = bracketed;
   {
     int lo_bit = 32;  // bits [lo_bit, 32) of the boundary key are known
@@ -255,7 +265,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
       for (int i = lane; i - lane < ncand; i += 32) {
         const uint32_t kk = i < ncand ? cand[i] : 0u;
         int bin = SEL_MAX_BINS;
-        if (i < ncand && (kk & mask) == prefix) bin = static_cast<int>((kk >> shift) & dmask);
+        if (i < ncand && kk <= cand_hi && (kk & mask) == prefix) bin = static_cast<int>((kk >> shift) & dmask);
         const unsigned peers = __match_any_sync(0xffffffffu, bin);
         if (bin < SEL_MAX_BINS && (peers & lt_mask) == 0) atomicAdd(&s_hist[bin], __popc(peers));
       }
@@ -309,19 +319,18 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
   }
   const uint32_t tau = ge_mode ? max(prefix, ge_floor) : prefix;
 
-  // Output: count this warp's kept keys (keys above the bracket are kept; the
-  // rest are in its region, else scan the whole range), scan the 32 warp
-  // totals, then place the kept ids in ascending u: key x goes to (#keys above
-  // tau before x) + min(#keys equal to tau before x, want), keeping the first
-  // `want` keys equal to tau.
+  // Output: count this warp's kept keys, scan the 32 warp totals, then place
+  // the kept ids in ascending u: key x goes to (#keys above tau before x) +
+  // min(#keys equal to tau before x, want), keeping the first `want` keys
+  // equal to tau.  With a bracket every kept key is in the warp's region
+  // (in range order, with its position); otherwise the whole range is read.
+  const uint32_t* ksrc = bracketed ? region : K + w0;
+  const int kn = bracketed ? w_cap : w1 - w0;
   int cg = 0, ce = 0;
-  const uint32_t* cnt_src = bracketed ? region : K + w0;
-  const int cnt_n = bracketed ? w_in : w1 - w0;
-  if (bracketed) cg = w_gt_hi;
 #pragma unroll 4
-  for (int i = lane; i - lane < cnt_n; i += 32) {
-    const bool live = i < cnt_n;
-    const uint32_t kk = live ? cnt_src[i] : 0u;
+  for (int i = lane; i - lane < kn; i += 32) {
+    const bool live = i < kn;
+    const uint32_t kk = live ? ksrc[i] : 0u;
     cg += __popc(__ballot_sync(0xffffffffu, live && (ge_mode ? (kk >= tau) : (kk > tau))));
     ce += __popc(__ballot_sync(0xffffffffu, live && !ge_mode && kk == tau));
   }
@@ -333,31 +342,38 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
   int tot_unused;
   int gtb = warp_totals_prefix(s_wgt, warp, lane, &tot_unused);
   int eqb = warp_totals_prefix(s_weq, warp, lane, &tot_unused);
-  for (int i0 = w0; i0 < w1; i0 += 32 * SEL_OUT_UNROLL) {
+  const int32_t* wsrc = src + w0;
+  for (int i0 = 0; i0 < kn; i0 += 32 * SEL_OUT_UNROLL) {
     uint32_t kk[SEL_OUT_UNROLL];
-    int id[SEL_OUT_UNROLL];
-#pragma unroll
-    for (int j = 0; j < SEL_OUT_UNROLL; ++j) {  // independent loads first
-      const int i = i0 + 32 * j + lane;
-      kk[j] = i < w1 ? K[i] : 0u;
-      id[j] = i < w1 ? __ldg(src + i) : -1;
-    }
+    int at[SEL_OUT_UNROLL];
 #pragma unroll
     for (int j = 0; j < SEL_OUT_UNROLL; ++j) {
-      const bool live = i0 + 32 * j + lane < w1;
+      const int i = i0 + 32 * j + lane;
+      kk[j] = i < kn ? ksrc[i] : 0u;
+      at[j] = i < kn ? (bracketed ? static_cast<int>(region_pos[i]) : i) : 0;
+    }
+    // kept keys and their output rows first, then the id loads of the kept ones
+    int pos[SEL_OUT_UNROLL];
+#pragma unroll
+    for (int j = 0; j < SEL_OUT_UNROLL; ++j) {
+      const bool live = i0 + 32 * j + lane < kn;
       const bool gt = live && (ge_mode ? (kk[j] >= tau) : (kk[j] > tau));
       const bool eq = live && !ge_mode && kk[j] == tau;
       const unsigned bg = __ballot_sync(0xffffffffu, gt);
       const unsigned be = __ballot_sync(0xffffffffu, eq);
       const int my_gt = gtb + __popc(bg & lt_mask);
       const int my_eq = eqb + __popc(be & lt_mask);
-      if (gt || (eq && my_eq < want)) {
-        const int pos = my_gt + min(my_eq, want);
-        if (pos < q_out) out[pos] = id[j];
-      }
+      pos[j] = (gt || (eq && my_eq < want)) ? my_gt + min(my_eq, want) : -1;
+      if (pos[j] >= q_out) pos[j] = -1;
       gtb += __popc(bg);
       eqb += __popc(be);
     }
+    int id[SEL_OUT_UNROLL];
+#pragma unroll
+    for (int j = 0; j < SEL_OUT_UNROLL; ++j) id[j] = pos[j] >= 0 ? __ldg(wsrc + at[j]) : 0;
+#pragma unroll
+    for (int j = 0; j < SEL_OUT_UNROLL; ++j)
+      if (pos[j] >= 0) out[pos[j]] = id[j];
   }
 }
 
@@ -386,7 +402,7 @@ extern "C" lrm_status lrm_select(lrm_ctx* ctx, const float* score, const int32_t
     if (p != nullptr && !aligned(p, 4)) return LRM_ERR_ALIGN;
   DeviceGuard guard(ctx->device);
   if (!guard.ok) return LRM_ERR_CUDA;
-  const size_t smem = (SEL_SMEM_KEYS + SEL_CAND_KEYS) * sizeof(uint32_t);
+  const size_t smem = (SEL_SMEM_KEYS + SEL_CAND_KEYS) * sizeof(uint32_t) + SEL_CAND_KEYS * sizeof(uint16_t);
   static thread_local int configured_device = -1;
   if (configured_device != ctx->device) {
     LRM_CHECK_CUDA(
