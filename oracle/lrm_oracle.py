@@ -51,6 +51,13 @@ __all__ = [
     "route_stats",
     "aux_loss",
     "score",
+    "score_metric",
+    "random_scores",
+    "splitmix64_outputs",
+    "METRIC_LRM",
+    "METRIC_GRAD_L2SQ",
+    "METRIC_GRAD_L1",
+    "METRIC_RANDOM",
     "select",
     "compact",
     "compact_padded",
@@ -199,6 +206,61 @@ def score(g_bits, phi_bits, alpha, k: int) -> np.ndarray:
     pn = np.einsum("ui,ui->u", phi, phi)
     t_of_u = np.arange(a.size) // k
     return a * a * gn[t_of_u] * pn
+
+
+# Selection metrics of LRMoE's ablation (sec. 4.7, Table 2).  The ablation
+# compares the LRM with a squared L2 norm of the gradient, an absolute
+# gradient magnitude and random drop; the gradient-only rules score a pair by
+# its token's upstream gradient g_t alone (sec. 4.7: two pairs with the same
+# upstream gradient norm get the same importance).  Readings: "|g|" is the L1
+# sum sum_i |g_t,i|; random drop scores every pair with an independent
+# uniform draw from the counter-based generator below.
+METRIC_LRM, METRIC_GRAD_L2SQ, METRIC_GRAD_L1, METRIC_RANDOM = 0, 1, 2, 3
+
+_M64 = (1 << 64) - 1
+_GOLDEN = 0x9E3779B97F4A7C15
+
+
+def splitmix64_outputs(state: int, count: int) -> list:
+    """The first `count` outputs of the SplitMix64 generator from `state`
+    (Steele, Lea and Flood, "Fast splittable pseudorandom number generators",
+    OOPSLA 2014): add the golden-ratio increment to the state, then mix with
+    two xor-shift-multiply steps and a final xor-shift."""
+    out = []
+    for _ in range(count):
+        state = (state + _GOLDEN) & _M64
+        z = state
+        z = ((z ^ (z >> 30)) * 0xBF58476D1CE4E5B9) & _M64
+        z = ((z ^ (z >> 27)) * 0x94D049BB133111EB) & _M64
+        out.append(z ^ (z >> 31))
+    return out
+
+
+def random_scores(seed: int, n: int) -> np.ndarray:
+    """Score of pair u: the (u+1)-th SplitMix64 output from state `seed`, top
+    24 bits as a uniform value in [0, 1) (exact in fp32 and fp64)."""
+    u = np.arange(n, dtype=np.uint64)
+    with np.errstate(over="ignore"):
+        z = (np.uint64(seed & _M64) + (u + np.uint64(1)) * np.uint64(_GOLDEN))
+        z = (z ^ (z >> np.uint64(30))) * np.uint64(0xBF58476D1CE4E5B9)
+        z = (z ^ (z >> np.uint64(27))) * np.uint64(0x94D049BB133111EB)
+        z = z ^ (z >> np.uint64(31))
+    return (z >> np.uint64(40)).astype(np.float64) * 2.0 ** -24
+
+
+def score_metric(metric: int, g_bits, phi_bits, alpha, k: int, seed: int = 0, n_pairs=None) -> np.ndarray:
+    """Per-pair selection score under one of the ablation's metrics."""
+    if metric == METRIC_LRM:
+        return score(g_bits, phi_bits, alpha, k)
+    if metric == METRIC_RANDOM:
+        n = int(n_pairs if n_pairs is not None else np.asarray(alpha).size)
+        return random_scores(seed, n)
+    g = bf16_to_f64(g_bits)
+    per_token = np.einsum("ti,ti->t", g, g) if metric == METRIC_GRAD_L2SQ else np.abs(g).sum(axis=1)
+    if metric not in (METRIC_GRAD_L2SQ, METRIC_GRAD_L1):
+        raise ValueError(f"unknown metric {metric}")
+    n = int(n_pairs if n_pairs is not None else g.shape[0] * k)
+    return per_token[np.arange(n) // k]
 
 
 # ---------------------------------------------------------------------------

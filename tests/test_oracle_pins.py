@@ -26,6 +26,57 @@ def _worked_example_routing(ex):
 
 
 # ---------------------------------------------------------------------------
+# selection metrics of the ablation (LRMoE sec. 4.7, Table 2)
+
+
+def test_splitmix64_reference_sequence(golden):
+    ref = golden("splitmix64_reference.json")
+    got = O.splitmix64_outputs(ref["state"], len(ref["outputs_hex"]))
+    assert got == [int(x, 16) for x in ref["outputs_hex"]]
+
+
+def test_random_scores_are_the_generator_outputs_and_uniform():
+    seed = 0x1234_5678_9ABC_DEF0
+    n = 1 << 16
+    r = O.random_scores(seed, n)
+    # the vectorised draw equals the sequential generator (24 top bits of output u+1)
+    seq = O.splitmix64_outputs(seed, 64)
+    assert np.array_equal(r[:64], np.array([x >> 40 for x in seq], dtype=np.float64) * 2.0 ** -24)
+    assert r.min() >= 0.0 and r.max() < 1.0
+    # fp32 holds every value exactly
+    assert np.array_equal(r.astype(np.float32).astype(np.float64), r)
+    counts = np.bincount((r * 64).astype(np.int64), minlength=64)
+    chi2 = ((counts - n / 64) ** 2 / (n / 64)).sum()
+    assert chi2 < 120  # 63 degrees of freedom: far above the 99.99th percentile is a broken generator
+    assert abs(np.corrcoef(r[:-1], r[1:])[0, 1]) < 0.02
+
+
+def test_gradient_metrics_hand_values():
+    g = f32_to_bf16_bits(np.array([[3.0, -4.0, 0.5, 0.0], [1.0, 1.0, 1.0, -1.0]], dtype=np.float32))
+    l2 = O.score_metric(O.METRIC_GRAD_L2SQ, g, None, None, k=2, n_pairs=4)
+    l1 = O.score_metric(O.METRIC_GRAD_L1, g, None, None, k=2, n_pairs=4)
+    assert l2.tolist() == [25.25, 25.25, 4.0, 4.0]
+    assert l1.tolist() == [7.5, 7.5, 4.0, 4.0]
+
+
+def test_l2_metric_is_the_lrm_with_unit_alpha_and_phi():
+    inp = generate("tiny_T256_E8_k2_h64_I32")
+    w = inp.workload
+    phi = np.zeros_like(inp.phi)
+    phi[:, 3] = f32_to_bf16_bits(np.array([1.0], dtype=np.float32))[0]
+    lrm = O.score(inp.g, phi, np.ones(w.N, dtype=np.float32), w.k)
+    l2 = O.score_metric(O.METRIC_GRAD_L2SQ, inp.g, None, None, w.k, n_pairs=w.N)
+    assert np.array_equal(lrm, l2)
+    # and the L1 metric scales linearly and ignores signs
+    g = inp.g.copy()
+    l1 = O.score_metric(O.METRIC_GRAD_L1, g, None, None, w.k, n_pairs=w.N)
+    g2 = g ^ np.uint16(0x8000)  # negate every bf16 value
+    assert np.array_equal(O.score_metric(O.METRIC_GRAD_L1, g2, None, None, w.k, n_pairs=w.N), l1)
+    g3 = f32_to_bf16_bits(2.0 * O.bf16_to_f64(g).astype(np.float32))
+    assert np.array_equal(O.score_metric(O.METRIC_GRAD_L1, g3, None, None, w.k, n_pairs=w.N), 2.0 * l1)
+
+
+# ---------------------------------------------------------------------------
 # routing statistics: "Expert Parallel Math Deep", worked example and aux range
 
 
