@@ -38,6 +38,19 @@ __device__ __forceinline__ void acc_sq8(const uint4& v, float (&a)[8]) {
   a[7] = fmaf(bf16_hi(v.w), bf16_hi(v.w), a[7]);
 }
 
+// Adds the magnitudes of the 8 bf16 values of v into 8 fp32 chains (the sign
+// bit cleared).
+__device__ __forceinline__ void acc_abs8(const uint4& v, float (&a)[8]) {
+  a[0] += bf16_lo(v.x & 0x7FFF7FFFu);
+  a[1] += bf16_hi(v.x & 0x7FFF7FFFu);
+  a[2] += bf16_lo(v.y & 0x7FFF7FFFu);
+  a[3] += bf16_hi(v.y & 0x7FFF7FFFu);
+  a[4] += bf16_lo(v.z & 0x7FFF7FFFu);
+  a[5] += bf16_hi(v.z & 0x7FFF7FFFu);
+  a[6] += bf16_lo(v.w & 0x7FFF7FFFu);
+  a[7] += bf16_hi(v.w & 0x7FFF7FFFu);
+}
+
 // bf16 pair (low, high) scaled by a: one fp32 multiply each, then
 // round-to-nearest-even to bf16.
 __device__ __forceinline__ uint32_t scale_bf16x2(uint32_t w, float a) {

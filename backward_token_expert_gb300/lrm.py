@@ -53,7 +53,11 @@ EXPORTED = (
     "lrm_set_wait_budget",
     "lrm_selftest_wait_timeout",
     "lrm_route_stats_noalloc",
+    "lrm_score_metric",
 )
+
+# selection metrics of lrm_score_metric (the ablation of LRMoE sec. 4.7, Table 2)
+METRIC_LRM, METRIC_GRAD_L2SQ, METRIC_GRAD_L1, METRIC_RANDOM = 0, 1, 2, 3
 
 # bytes of the library's fixed scratch array used by lrm_route_stats_noalloc
 ROUTE_STATS_SCRATCH_BYTES = 4 << 20
@@ -124,6 +128,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "lrm_set_wait_budget": ([P, ctypes.c_uint64], st),
         "lrm_selftest_wait_timeout": ([P, ctypes.c_uint64, P], st),
         "lrm_route_stats_noalloc": ([P, P, P, Dims, i32, i32, i32, i32, P, P, P, P, P, P, P, P], st),
+        "lrm_score_metric": ([P, i32, P, P, P, Dims, ctypes.c_uint64, P, P], st),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -221,6 +226,12 @@ def lrm_route_stats_noalloc(ctx, logits, expert_idx, dims: Dims, cf, rho, counts
 def lrm_score(ctx, g, phi, alpha, dims: Dims, score, stream=None) -> None:
     _check(load_library().lrm_score(ctx, _ptr(g), _ptr(phi), _ptr(alpha), dims, _ptr(score), _stream(stream)),
            "lrm_score")
+
+
+def lrm_score_metric(ctx, metric: int, g, phi, alpha, dims: Dims, seed: int, score, stream=None) -> None:
+    _check(load_library().lrm_score_metric(ctx, int(metric), _ptr(g), _ptr(phi), _ptr(alpha), dims,
+                                           int(seed) & ((1 << 64) - 1), _ptr(score), _stream(stream)),
+           "lrm_score_metric")
 
 
 def lrm_select(ctx, score, offsets, bucket, quota, dims: Dims, max_rows: int, sel_offsets, sel_ids, ws=None,

@@ -123,8 +123,13 @@ class Recalibration:
         if quota_override is not None:
             b.quota.copy_(quota_override)
 
-    def score(self, g, phi, alpha, stream=None):
-        L.lrm_score(self.ctx, g, phi, alpha, self.dims, self.buf.score, stream)
+    def score(self, g, phi, alpha, stream=None, metric: int = L.METRIC_LRM, seed: int = 0):
+        """Step 2.  `metric` selects the LRM (default) or one of the ablation's
+        alternatives (gradient L2, gradient L1, seeded random)."""
+        if metric == L.METRIC_LRM:
+            L.lrm_score(self.ctx, g, phi, alpha, self.dims, self.buf.score, stream)
+        else:
+            L.lrm_score_metric(self.ctx, metric, g, phi, alpha, self.dims, seed, self.buf.score, stream)
 
     def select(self, stream=None, score=None):
         b = self.buf
@@ -145,9 +150,9 @@ class Recalibration:
         L.lrm_grouped_wgrad(self.ctx, b.delta_c, b.phi_c, b.sel_offsets, self.dims, self.max_rows, accumulate,
                             b.dW, stream)
 
-    def backward_steps(self, g, phi, alpha, W, stream=None):
+    def backward_steps(self, g, phi, alpha, W, stream=None, metric: int = L.METRIC_LRM, seed: int = 0):
         """score -> select -> compact -> dgrad -> wgrad (quotas already set)."""
-        self.score(g, phi, alpha, stream)
+        self.score(g, phi, alpha, stream, metric=metric, seed=seed)
         self.select(stream)
         self.compact(g, phi, alpha, stream)
         self.dgrad(W, stream)

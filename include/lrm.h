@@ -155,6 +155,29 @@ LRM_API lrm_status lrm_score(lrm_ctx* ctx, const uint16_t* g, const uint16_t* ph
                      lrm_dims dims, float* score, void* stream);
 
 /*
+ * Step 2 with the selection metrics of LRMoE's ablation (sec. 4.7, Table 2),
+ * for comparing selection rules on the same pairs:
+ *   LRM_METRIC_LRM       the Load Recalibration Metric (same as lrm_score)
+ *   LRM_METRIC_GRAD_L2SQ score[u] = ||g_t||^2 (gradient only)
+ *   LRM_METRIC_GRAD_L1   score[u] = sum_i |g_t,i| (gradient only; the
+ *                        ablation's "|g|" read as an L1 sum)
+ *   LRM_METRIC_RANDOM    score[u] = top 24 bits of the (u+1)-th output of the
+ *                        SplitMix64 generator (Steele, Lea and Flood, OOPSLA
+ *                        2014) started from state `seed`, times 2^-24
+ * phi and alpha are read only by LRM_METRIC_LRM, g by every metric but
+ * LRM_METRIC_RANDOM (unused pointers may be NULL).  fp32 accumulation as in
+ * lrm_score.  An unknown metric returns LRM_ERR_INVALID_ARG.
+ */
+typedef enum lrm_metric {
+  LRM_METRIC_LRM = 0,
+  LRM_METRIC_GRAD_L2SQ = 1,
+  LRM_METRIC_GRAD_L1 = 2,
+  LRM_METRIC_RANDOM = 3
+} lrm_metric;
+LRM_API lrm_status lrm_score_metric(lrm_ctx* ctx, int32_t metric, const uint16_t* g, const uint16_t* phi,
+                            const float* alpha, lrm_dims dims, uint64_t seed, float* score, void* stream);
+
+/*
  * Step 3 - per-expert TopK within the quota (LRMoE sec. 3.2, Alg. 1 line 14,
  * appendix 7.2 Prop. 7.1): for every expert e keep the quota[e] pairs of
  * bucket[offsets[e] .. offsets[e+1]) with the largest score; equal scores go

@@ -42,7 +42,7 @@ def workload(base="tiny_T256_E8_k2_h64_I32", **kw):
     return get_workload(base, **kw)
 
 
-def run_gpu(inp, cf=None, rho=None, quota=None, max_rows=None, padded=False):
+def run_gpu(inp, cf=None, rho=None, quota=None, max_rows=None, padded=False, metric=0, seed=0):
     """Run the whole path on cuda:0; returns numpy copies of every output."""
     from backward_token_expert_gb300 import lrm as L
     from backward_token_expert_gb300.pipeline import Recalibration, to_device_inputs
@@ -57,7 +57,7 @@ def run_gpu(inp, cf=None, rho=None, quota=None, max_rows=None, padded=False):
         d = to_device_inputs(inp)
         q = None if quota is None else torch.as_tensor(np.asarray(quota, dtype=np.int32), device="cuda")
         rec.route_stats(d["logits"], d["expert_idx"], quota_override=q)
-        rec.backward_steps(d["g"], d["phi"], d["alpha"], d["W"])
+        rec.backward_steps(d["g"], d["phi"], d["alpha"], d["W"], metric=metric, seed=seed)
         torch.cuda.synchronize()
         b = rec.buf
         so = b.sel_offsets.cpu().numpy().astype(np.int64)

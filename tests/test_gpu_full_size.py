@@ -91,3 +91,23 @@ def test_skew_sweep_corners():
 def test_large_batch_stress_with_empty_and_oversized_experts():
     inp, gpu, st, _ = sampled_check("stress_T131072_E128_k8_h4096_I1408", n_random_experts=2)
     assert (st["counts"] == 0).sum() >= 1 and (st["counts"] > st["C"]).sum() >= 1
+
+
+def test_deepseek_v2_layer():
+    # E = 160 and k = 6: no power of two in the expert count, the pair count
+    # per token or the per-block token count of route stats; h = 5120
+    inp, gpu, st, _ = sampled_check("deepseek_v2_T32768_E160_k6_h5120_I1536")
+    assert (st["counts"] > st["C"]).sum() >= 1
+
+
+def test_gradient_l2_metric_at_full_size():
+    # the ablation's gradient-only rule through the whole path of the bench workload
+    from gpu_common import check_selection
+
+    inp = generate("qwen3_30b_a3b_T32768_E128_k8_h2048_I768")
+    w = inp.workload
+    gpu = run_gpu(inp, metric=O.METRIC_GRAD_L2SQ)
+    st = O.route_stats(inp.logits, inp.expert_idx, w.E, w.cf, w.rho)
+    R = O.score_metric(O.METRIC_GRAD_L2SQ, inp.g, None, None, w.k, n_pairs=w.N)
+    assert np.all(rel_close(gpu["score"], R, SCORE_RTOL, 1e-30))
+    check_selection(gpu, inp, st["quota"])

@@ -75,6 +75,8 @@ for _s in (0.0, 0.8, 1.2, 1.6):
                  _s, _rho, note="skew/retention sweep on Qwen3-30B-A3B shapes"))
 _add(_wl("stress_T131072_E128_k8_h4096_I1408", 131072, 128, 8, 4096, 1408, 1.2, Fraction(1, 2),
          dead_experts=2, note="large batch with empty and over-capacity experts"))
+_add(_wl("deepseek_v2_T32768_E160_k6_h5120_I1536", 32768, 160, 6, 5120, 1536, 1.0, Fraction(3, 4),
+         note="DeepSeek-V2-shaped layer: E = 160 and k = 6 are not powers of two, wider h"))
 
 
 def get_workload(name: str, **overrides) -> Workload:
