@@ -64,6 +64,7 @@ __all__ = [
     "grouped_wgrad",
     "grouped_dgrad",
     "grouped_wgrad_from_compact",
+    "scatter_with_zeros",
     "grouped_dgrad_from_compact",
     "backward_recalibration",
 ]
@@ -372,6 +373,19 @@ def grouped_dgrad(g_bits, W_bits, alpha, sel_offsets, sel_ids, E: int, k: int, e
         ids = ids_all[so[e]:so[e + 1]]
         d = a[ids][:, None] * bf16_to_f64(g_bits[ids // k])
         out[e] = d @ bf16_to_f64(W_bits[e])
+    return out
+
+
+def scatter_with_zeros(rows, sel_ids, N: int) -> np.ndarray:
+    """The inverse mapping of LRMoE (sec. 1 and 3.3; Alg. 1 line 19,
+    ScatterWithZeros; sec. 3.4: retained results go back to their original
+    positions and zeros are restored before the next dense-layer boundary):
+    row r of `rows` (the r-th retained pair in the compacted order) goes to
+    row sel_ids[r] of an [N, width] array whose other rows are zero."""
+    rows = np.asarray(rows)
+    ids = np.asarray(sel_ids, dtype=np.int64)
+    out = np.zeros((N,) + rows.shape[1:], dtype=rows.dtype)
+    out[ids] = rows
     return out
 
 

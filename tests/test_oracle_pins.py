@@ -387,6 +387,34 @@ def test_full_retention_equals_dense_moe_fc2_gradient():
         assert np.allclose(dphi[e], dense_dphi[seg], rtol=1e-12, atol=1e-14)
 
 
+def test_scatter_with_zeros_is_the_dense_input_gradient_with_dropped_rows_zero():
+    """The inverse mapping puts every retained row back at its pair: with full
+    retention it equals the dense MoE FC2 input gradient written with a one-hot
+    dispatch tensor; with a quota, the retained rows equal that dense gradient
+    and every dropped row is zero."""
+    T, k, E, h, I = 12, 2, 4, 6, 5
+    g, phi, W, alpha, idx = _tiny(T=T, k=k, E=E, h=h, I=I, seed=9)
+    N = T * k
+    onehot = np.zeros((N, E))
+    onehot[np.arange(N), idx.reshape(-1)] = 1.0
+    gu = O.bf16_to_f64(g)[np.arange(N) // k]
+    dense = np.einsum("ue,u,ui,eij->uj", onehot, alpha.astype(np.float64), gu, O.bf16_to_f64(W))
+    logits = np.zeros((T, E), np.float32)
+    for rho, cf in ((Fraction(1), Fraction(4)), (Fraction(1, 2), Fraction(5, 4))):
+        st = O.route_stats(logits, idx, E, cf=cf, rho=rho)
+        so, ids = O.select(O.score(g, phi, alpha, k), idx, E, st["quota"])
+        dphi = O.grouped_dgrad(g, W, alpha, so, ids, E, k)
+        rows = np.concatenate([dphi[e] for e in range(E)], axis=0)
+        out = O.scatter_with_zeros(rows, ids, N)
+        kept = np.zeros(N, dtype=bool)
+        kept[ids] = True
+        assert np.allclose(out[kept], dense[kept], rtol=1e-12, atol=1e-14)
+        assert np.all(out[~kept] == 0.0)
+        assert kept.sum() == st["retained"]
+        if rho == 1:
+            assert kept.all() and np.allclose(out, dense, rtol=1e-12, atol=1e-14)
+
+
 def test_zero_masked_layout_gives_same_gradients():
     """Sec. 3.4: the zero-masked fixed-shape computation equals the compacted one."""
     T, k, E = 16, 2, 4
