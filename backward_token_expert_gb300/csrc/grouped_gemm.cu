@@ -527,7 +527,8 @@ template <int BNR>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CfgDgradPair<BNR>::THREADS, 1)
     dgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const int32_t* __restrict__ sel_offsets, int E, int h, int I, int max_rows,
-                      uint16_t* __restrict__ out, unsigned int* status, unsigned long long budget_ns) {
+                      uint16_t* __restrict__ out, const int32_t* __restrict__ row_map, int out_rows,
+                      unsigned int* status, unsigned long long budget_ns) {
   using C = CfgDgradPair<BNR>;
   extern __shared__ uint8_t dsmem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsmem_raw) + 1023) & ~uintptr_t(1023));
@@ -754,7 +755,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CfgDgradPair<BNR>::T
       }
       tc_fence_after();
       const int col0 = mt * 256 + static_cast<int>(rank) * 128 + q * 32;  // first I column of this warp
-      uint16_t* obase = out + static_cast<size_t>(start + nt * BNR) * I + col0;
+      const int row0 = start + nt * BNR;  // first compacted row of this tile
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BNR;
       const int c_end = min(n_cols, c_begin + BNR / 2);
       for (int c = c_begin; c < c_end; c += 32) {
@@ -771,11 +772,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CfgDgradPair<BNR>::T
         }
         __syncwarp();
         if (c + lane < rows_valid) {  // lane = output row c + lane
-          const uint4* src = reinterpret_cast<const uint4*>(tbuf + lane * C::T_PITCH);
-          uint16_t* orow = obase + static_cast<size_t>(c + lane) * I;
+          // compacted layout: row r of out; with a row map (the inverse mapping
+          // of the selection), row row_map[r] of the [out_rows, I] array
+          int r = row0 + c + lane;
+          if (row_map != nullptr) {
+            r = __ldg(row_map + r);
+            if (r < 0 || r >= out_rows) {
+              raise_flag(status, LRM_ERR_INDEX);
+              r = -1;
+            }
+          }
+          if (r >= 0) {
+            const uint4* src = reinterpret_cast<const uint4*>(tbuf + lane * C::T_PITCH);
+            uint16_t* orow = out + static_cast<size_t>(r) * I + col0;
 #pragma unroll
-          for (int v = 0; v < 4; ++v)
-            if (col0 + v * 8 < I) *reinterpret_cast<uint4*>(orow + v * 8) = src[(v ^ (lane >> 1)) & 3];
+            for (int v = 0; v < 4; ++v)
+              if (col0 + v * 8 < I) *reinterpret_cast<uint4*>(orow + v * 8) = src[(v ^ (lane >> 1)) & 3];
+          }
         }
       }
       tc_fence_before();
@@ -852,7 +865,8 @@ lrm_status launch_wgrad_pair(lrm_ctx* ctx, const CUtensorMap& a, const CUtensorM
 // a = W_e^T operand (W map), b = segment rows operand (delta_c map)
 template <int BNR>
 lrm_status launch_dgrad_pair(lrm_ctx* ctx, const CUtensorMap& a, const CUtensorMap& b, const int32_t* sel_offsets,
-                             const lrm_dims& d, int max_rows, uint16_t* out, cudaStream_t s) {
+                             const lrm_dims& d, int max_rows, uint16_t* out, const int32_t* row_map, int out_rows,
+                             cudaStream_t s) {
   using C = CfgDgradPair<BNR>;
   auto kern = dgrad_pair_kernel<BNR>;
   static thread_local int configured_device = -1;
@@ -870,8 +884,8 @@ lrm_status launch_dgrad_pair(lrm_ctx* ctx, const CUtensorMap& a, const CUtensorM
     clusters = n;
     configured_device = ctx->device;
   }
-  kern<<<2 * clusters, C::THREADS, C::SMEM_BYTES, s>>>(a, b, sel_offsets, d.E, d.h, d.I, max_rows, out,
-                                                       ctx->d_status, ctx->wait_budget_ns);
+  kern<<<2 * clusters, C::THREADS, C::SMEM_BYTES, s>>>(a, b, sel_offsets, d.E, d.h, d.I, max_rows, out, row_map,
+                                                       out_rows, ctx->d_status, ctx->wait_budget_ns);
   return launch_status();
 }
 
@@ -880,16 +894,21 @@ lrm_status launch_dgrad_pair(lrm_ctx* ctx, const CUtensorMap& a, const CUtensorM
 
 using namespace lrm;
 
-extern "C" lrm_status lrm_grouped_dgrad(lrm_ctx* ctx, const uint16_t* delta_c, const uint16_t* W,
-                                        const int32_t* sel_offsets, lrm_dims dims, int32_t max_rows,
-                                        uint16_t* dphi_c, void* stream) {
+namespace {
+
+// Both dgrad entry points: rows go to `out` in the compacted order, or through
+// `row_map` to rows of an [out_rows, I] array.
+lrm_status grouped_dgrad(lrm_ctx* ctx, const uint16_t* delta_c, const uint16_t* W, const int32_t* sel_offsets,
+                         lrm_dims dims, int32_t max_rows, uint16_t* out, const int32_t* row_map, int out_rows,
+                         void* stream) {
   if (ctx == nullptr) return LRM_ERR_INVALID_ARG;
   lrm_status st = check_dims(dims);
   if (st != LRM_OK) return st;
   if (max_rows < 0 || sel_offsets == nullptr) return LRM_ERR_INVALID_ARG;
   if (max_rows == 0) return LRM_OK;
-  if (delta_c == nullptr || W == nullptr || dphi_c == nullptr) return LRM_ERR_INVALID_ARG;
-  if (!aligned(delta_c, 16) || !aligned(W, 16) || !aligned(dphi_c, 16) || !aligned(sel_offsets, 4))
+  if (delta_c == nullptr || W == nullptr || out == nullptr) return LRM_ERR_INVALID_ARG;
+  if (!aligned(delta_c, 16) || !aligned(W, 16) || !aligned(out, 16) || !aligned(sel_offsets, 4) ||
+      (row_map != nullptr && !aligned(row_map, 4)))
     return LRM_ERR_ALIGN;
   DeviceGuard guard(ctx->device);
   if (!guard.ok) return LRM_ERR_CUDA;
@@ -898,7 +917,22 @@ extern "C" lrm_status lrm_grouped_dgrad(lrm_ctx* ctx, const uint16_t* delta_c, c
   if ((st = encode_2d(ctx, &ma, delta_c, dims.h, max_rows, 256 / 2)) != LRM_OK) return st;
   if ((st = encode_w(ctx, &mb, W, dims.I, dims.h, dims.E, CD::BKS)) != LRM_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return launch_dgrad_pair<256>(ctx, mb, ma, sel_offsets, dims, max_rows, dphi_c, s);
+  return launch_dgrad_pair<256>(ctx, mb, ma, sel_offsets, dims, max_rows, out, row_map, out_rows, s);
+}
+
+}  // namespace
+
+extern "C" lrm_status lrm_grouped_dgrad(lrm_ctx* ctx, const uint16_t* delta_c, const uint16_t* W,
+                                        const int32_t* sel_offsets, lrm_dims dims, int32_t max_rows,
+                                        uint16_t* dphi_c, void* stream) {
+  return grouped_dgrad(ctx, delta_c, W, sel_offsets, dims, max_rows, dphi_c, nullptr, 0, stream);
+}
+
+extern "C" lrm_status lrm_grouped_dgrad_scatter(lrm_ctx* ctx, const uint16_t* delta_c, const uint16_t* W,
+                                                const int32_t* sel_offsets, const int32_t* sel_ids, lrm_dims dims,
+                                                int32_t max_rows, uint16_t* dphi_rows, void* stream) {
+  if (sel_ids == nullptr && max_rows > 0) return LRM_ERR_INVALID_ARG;
+  return grouped_dgrad(ctx, delta_c, W, sel_offsets, dims, max_rows, dphi_rows, sel_ids, dims.T * dims.k, stream);
 }
 
 extern "C" lrm_status lrm_grouped_wgrad(lrm_ctx* ctx, const uint16_t* delta_c, const uint16_t* phi_c,

@@ -33,6 +33,7 @@ STATUS_NAMES = [
  LRM_ERR_TIMEOUT, LRM_ERR_ARCH, LRM_ERR_CUDA) = range(1, 10)
 LRM_OP_ROUTE_STATS = 0
 LRM_OP_SELECT = 1
+LRM_OP_ZERO_DROPPED = 2
 
 # every entry point declared in include/lrm.h
 EXPORTED = (
@@ -54,6 +55,8 @@ EXPORTED = (
     "lrm_selftest_wait_timeout",
     "lrm_route_stats_noalloc",
     "lrm_score_metric",
+    "lrm_grouped_dgrad_scatter",
+    "lrm_zero_dropped_rows",
 )
 
 # selection metrics of lrm_score_metric (the ablation of LRMoE sec. 4.7, Table 2)
@@ -129,6 +132,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "lrm_selftest_wait_timeout": ([P, ctypes.c_uint64, P], st),
         "lrm_route_stats_noalloc": ([P, P, P, Dims, i32, i32, i32, i32, P, P, P, P, P, P, P, P], st),
         "lrm_score_metric": ([P, i32, P, P, P, Dims, ctypes.c_uint64, P, P], st),
+        "lrm_grouped_dgrad_scatter": ([P, P, P, P, P, Dims, i32, P, P], st),
+        "lrm_zero_dropped_rows": ([P, P, P, Dims, i32, P, P, ctypes.c_size_t, P], st),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -232,6 +237,20 @@ def lrm_score_metric(ctx, metric: int, g, phi, alpha, dims: Dims, seed: int, sco
     _check(load_library().lrm_score_metric(ctx, int(metric), _ptr(g), _ptr(phi), _ptr(alpha), dims,
                                            int(seed) & ((1 << 64) - 1), _ptr(score), _stream(stream)),
            "lrm_score_metric")
+
+
+def lrm_grouped_dgrad_scatter(ctx, delta_c, W, sel_offsets, sel_ids, dims: Dims, max_rows: int, dphi_rows,
+                              stream=None) -> None:
+    _check(load_library().lrm_grouped_dgrad_scatter(ctx, _ptr(delta_c), _ptr(W), _ptr(sel_offsets), _ptr(sel_ids),
+                                                    dims, int(max_rows), _ptr(dphi_rows), _stream(stream)),
+           "lrm_grouped_dgrad_scatter")
+
+
+def lrm_zero_dropped_rows(ctx, sel_offsets, sel_ids, dims: Dims, max_rows: int, rows, ws, ws_bytes: int,
+                          stream=None) -> None:
+    _check(load_library().lrm_zero_dropped_rows(ctx, _ptr(sel_offsets), _ptr(sel_ids), dims, int(max_rows),
+                                                _ptr(rows), _ptr(ws), int(ws_bytes), _stream(stream)),
+           "lrm_zero_dropped_rows")
 
 
 def lrm_select(ctx, score, offsets, bucket, quota, dims: Dims, max_rows: int, sel_offsets, sel_ids, ws=None,

@@ -145,6 +145,20 @@ class Recalibration:
         b = self.buf
         L.lrm_grouped_dgrad(self.ctx, b.delta_c, W, b.sel_offsets, self.dims, self.max_rows, b.dphi_c, stream)
 
+    def dgrad_scatter(self, W, dphi_rows, stream=None, zero_dropped: bool = True):
+        """Step 5a with the inverse mapping: the input gradient of every
+        retained pair goes to its row of `dphi_rows` ([N, I] bf16, the layout
+        of phi); with `zero_dropped` the rows of the other pairs become zeros."""
+        b = self.buf
+        L.lrm_grouped_dgrad_scatter(self.ctx, b.delta_c, W, b.sel_offsets, b.sel_ids, self.dims, self.max_rows,
+                                    dphi_rows, stream)
+        if zero_dropped:
+            if getattr(self, "_ws_zero", None) is None:
+                nbytes = L.lrm_workspace_size(self.ctx, L.LRM_OP_ZERO_DROPPED, self.dims)
+                self._ws_zero = torch.empty(max(nbytes, 4), dtype=torch.uint8, device=self.buf.dW.device)
+            L.lrm_zero_dropped_rows(self.ctx, b.sel_offsets, b.sel_ids, self.dims, self.max_rows, dphi_rows,
+                                    self._ws_zero, self._ws_zero.numel(), stream)
+
     def wgrad(self, stream=None, accumulate=0):
         b = self.buf
         L.lrm_grouped_wgrad(self.ctx, b.delta_c, b.phi_c, b.sel_offsets, self.dims, self.max_rows, accumulate,

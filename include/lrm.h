@@ -72,7 +72,7 @@ typedef enum lrm_status {
 } lrm_status;
 
 /* Operations that take a workspace, for lrm_workspace_size. */
-typedef enum lrm_op { LRM_OP_ROUTE_STATS = 0, LRM_OP_SELECT = 1 } lrm_op;
+typedef enum lrm_op { LRM_OP_ROUTE_STATS = 0, LRM_OP_SELECT = 1, LRM_OP_ZERO_DROPPED = 2 } lrm_op;
 
 /* Layer sizes.  Limits: 1 <= E <= 1024, 1 <= k <= 32, k <= E, N = T*k < 2^31,
  * h and I multiples of 8 in [8, 65536]. */
@@ -220,6 +220,30 @@ LRM_API lrm_status lrm_compact(lrm_ctx* ctx, const uint16_t* g, const uint16_t* 
 LRM_API lrm_status lrm_grouped_dgrad(lrm_ctx* ctx, const uint16_t* delta_c, const uint16_t* W,
                              const int32_t* sel_offsets, lrm_dims dims, int32_t max_rows,
                              uint16_t* dphi_c, void* stream);
+
+/*
+ * The inverse mapping (LRMoE sec. 1 and 3.3; Alg. 1 line 19, ScatterWithZeros;
+ * sec. 3.4: retained results go back to their original positions, zeros are
+ * restored before the next dense-layer boundary), in two calls:
+ *
+ * lrm_grouped_dgrad_scatter: step 5a with the rows written through the
+ * selection: the input-gradient row of retained pair u = sel_ids[r] goes to
+ * row u of dphi_rows [N, I] bf16 (the pair-major layout of phi) instead of row
+ * r of the compacted output.  The values are those of lrm_grouped_dgrad bit
+ * for bit.  Rows of pairs that were not retained are not written.  A sel_ids
+ * entry outside [0, N) sets LRM_ERR_INDEX and its row is skipped.
+ *
+ * lrm_zero_dropped_rows: writes zeros to every row u of rows [N, I] bf16 whose
+ * pair is not among sel_ids[0 .. sel_offsets[E]) (clamped to max_rows).  ws:
+ * an N-bit map (lrm_workspace_size with LRM_OP_ZERO_DROPPED), cleared on the
+ * stream by the call.  The two calls write disjoint rows, in either order.
+ */
+LRM_API lrm_status lrm_grouped_dgrad_scatter(lrm_ctx* ctx, const uint16_t* delta_c, const uint16_t* W,
+                                     const int32_t* sel_offsets, const int32_t* sel_ids, lrm_dims dims,
+                                     int32_t max_rows, uint16_t* dphi_rows, void* stream);
+LRM_API lrm_status lrm_zero_dropped_rows(lrm_ctx* ctx, const int32_t* sel_offsets, const int32_t* sel_ids,
+                                 lrm_dims dims, int32_t max_rows, uint16_t* rows, void* ws, size_t ws_bytes,
+                                 void* stream);
 
 /*
  * Step 5b - grouped FC2 weight gradient, variable K, no padding (LRMoE
