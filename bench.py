@@ -340,6 +340,7 @@ def run_ours(args, rank, world, local):
         }
         if not args.no_comparator:
             result["comparator"] = comparator(rec, d, w, retained, pk)
+            result["inverse_mapping"] = inverse_mapping(rec, d, w, retained, pk)
         if not args.no_cpu_baseline:
             result["cpu_baseline"] = cpu_baseline(inp, tokens=args.ref_tokens or 8192)
     if not args.no_e2e:
@@ -354,6 +355,38 @@ def run_ours(args, rank, world, local):
         dist.barrier()
         dist.destroy_process_group()
     return result
+
+
+def inverse_mapping(rec, d, w, retained, pk, iters=20):
+    """The inverse mapping (ScatterWithZeros): dgrad written through the
+    selection into the [N, I] pair-major layout plus the zeroing of the dropped
+    rows, against the compacted dgrad alone."""
+    import torch
+
+    rows = torch.empty(w.N, w.I, dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.current_stream()
+    out = {}
+    for name, fn in (("dgrad_compacted", lambda: rec.dgrad(d["W"])),
+                     ("dgrad_scatter", lambda: rec.dgrad_scatter(d["W"], rows, zero_dropped=False)),
+                     ("scatter_with_zeros", lambda: rec.dgrad_scatter(d["W"], rows, zero_dropped=True))):
+        for _ in range(3):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(iters):
+            fn()
+        e1.record(s)
+        e1.synchronize()
+        out[name + "_ms"] = round(e0.elapsed_time(e1) / iters, 5)
+    zero_bytes = (w.N - retained) * w.I * 2
+    out.update(what="dgrad into the compacted rows vs through the selection into [N, I] (+ zeros for dropped rows)",
+               zeroed_bytes=zero_bytes,
+               zeroing_hbm_frac=round(zero_bytes / (pk["hbm"] * 1e9) /
+                                      max((out["scatter_with_zeros_ms"] - out["dgrad_scatter_ms"]) * 1e-3, 1e-9), 4))
+    flags = rec.device_status()
+    if flags:
+        raise RuntimeError(f"device status flags {flags:#x} in the inverse mapping")
+    return out
 
 
 def comparator(rec, d, w, retained, pk, iters=20):
