@@ -65,6 +65,11 @@ __all__ = [
     "grouped_dgrad",
     "grouped_wgrad_from_compact",
     "scatter_with_zeros",
+    "silu",
+    "swiglu_forward",
+    "swiglu_backward",
+    "fc1_backward",
+    "combine_pairs",
     "grouped_dgrad_from_compact",
     "backward_recalibration",
 ]
@@ -386,6 +391,71 @@ def scatter_with_zeros(rows, sel_ids, N: int) -> np.ndarray:
     ids = np.asarray(sel_ids, dtype=np.int64)
     out = np.zeros((N,) + rows.shape[1:], dtype=rows.dtype)
     out[ids] = rows
+    return out
+
+
+# ---------------------------------------------------------------------------
+# FC1 and its activation on the retained pairs (LRMoE sec. 3.4: compaction
+# reduces the row dimension of all four expert-backward GEMMs, the FC1 and
+# FC2 data- and weight-gradient operations).  The pages do not name the
+# activation; it is read as SwiGLU: FC1 maps the expert input x_t to
+# [a_u ; b_u] = W1_e x_t (W1_e is [2I, h], gate rows first), and the FC2
+# input is phi_u = silu(a_u) * b_u with silu(a) = a / (1 + exp(-a)).
+
+
+def silu(a):
+    return a / (1.0 + np.exp(-a))
+
+
+def swiglu_forward(ab):
+    """phi = silu(a) * b for rows [a | b] of width 2I."""
+    ab = np.asarray(ab, dtype=np.float64)
+    I = ab.shape[1] // 2
+    return silu(ab[:, :I]) * ab[:, I:]
+
+
+def swiglu_backward(dphi, ab):
+    """[da | db] for rows of phi = silu(a) * b: db = dphi * silu(a) and
+    da = dphi * b * silu'(a), silu'(a) = s (1 + a (1 - s)), s = 1 / (1 + exp(-a))."""
+    dphi = np.asarray(dphi, dtype=np.float64)
+    ab = np.asarray(ab, dtype=np.float64)
+    I = ab.shape[1] // 2
+    a, b = ab[:, :I], ab[:, I:]
+    sg = 1.0 / (1.0 + np.exp(-a))
+    return np.concatenate([dphi * b * sg * (1.0 + a * (1.0 - sg)), dphi * a * sg], axis=1)
+
+
+def fc1_backward(x, ab, W1, dphi_rows, sel_offsets, sel_ids, E: int, k: int, experts=None):
+    """FC1 weight and input gradients of the retained pairs of every expert.
+
+    x [T, h], ab [N, 2I] (the saved FC1 outputs [a | b] of every pair) and W1
+    [E, 2I, h] are real arrays (convert bf16 bits with bf16_to_f64 first).
+    dphi_rows[r] is the FC2 input gradient of the r-th retained pair (the
+    compacted order).  For pair u = sel_ids[r] of expert e, token t = u div k:
+    dh1_u = swiglu_backward(dphi_u, [a_u | b_u]); dW1_e = sum_u dh1_u x_t^T
+    ([2I, h]); dx_u = W1_e^T dh1_u ([h]).  Returns ({e: dW1_e}, dx_rows) with
+    dx_rows in the compacted order (rows of experts not in `experts` are 0).
+    """
+    so = np.asarray(sel_offsets, dtype=np.int64)
+    ids_all = np.asarray(sel_ids, dtype=np.int64)
+    x = np.asarray(x, dtype=np.float64)
+    dh1 = swiglu_backward(dphi_rows, np.asarray(ab, dtype=np.float64)[ids_all])
+    dW1 = {}
+    dx = np.zeros((ids_all.size, x.shape[1]))
+    for e in range(E) if experts is None else experts:
+        r0, r1 = so[e], so[e + 1]
+        dW1[e] = dh1[r0:r1].T @ x[ids_all[r0:r1] // k]
+        dx[r0:r1] = dh1[r0:r1] @ np.asarray(W1[e], dtype=np.float64)
+    return dW1, dx
+
+
+def combine_pairs(rows, sel_ids, T: int, k: int) -> np.ndarray:
+    """Input gradient of every token: the sum of the rows of its retained
+    pairs (the inverse mapping followed by the MoE combine over the token's k
+    experts); tokens without a retained pair get zeros."""
+    rows = np.asarray(rows, dtype=np.float64)
+    out = np.zeros((T, rows.shape[1]))
+    np.add.at(out, np.asarray(sel_ids, dtype=np.int64) // k, rows)
     return out
 
 

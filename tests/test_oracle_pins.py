@@ -509,3 +509,80 @@ def test_full_oracle_pass_on_tiny_workload():
     assert st["C"] == 80 and st["counts"].sum() == 512
     assert np.all(np.diff(out["sel_offsets"]) == st["quota"])
     assert out["delta_c"].shape == (st["retained"], 64)
+
+
+# ---------------------------------------------------------------------------
+# FC1 and its activation (LRMoE sec. 3.4: all four expert-backward GEMMs run on
+# the retained rows; the activation is read as SwiGLU)
+
+
+def test_swiglu_backward_matches_autograd_and_finite_differences():
+    import torch
+
+    rng = np.random.default_rng(41)
+    ab = rng.standard_normal((7, 10)) * 2.0
+    dphi = rng.standard_normal((7, 5))
+    t_ab = torch.tensor(ab, dtype=torch.float64, requires_grad=True)
+    a, b = t_ab[:, :5], t_ab[:, 5:]
+    (torch.tensor(dphi) * (torch.nn.functional.silu(a) * b)).sum().backward()
+    assert np.allclose(O.swiglu_backward(dphi, ab), t_ab.grad.numpy(), rtol=1e-12, atol=1e-14)
+    assert np.allclose(O.swiglu_forward(ab), (torch.nn.functional.silu(a) * b).detach().numpy(), rtol=1e-14)
+    # silu'(a) against a central difference of silu
+    x = np.linspace(-8, 8, 33)
+    h = 1e-6
+    num = (O.silu(x + h) - O.silu(x - h)) / (2 * h)
+    ana = O.swiglu_backward(np.ones((33, 1)), np.stack([x, np.ones(33)], axis=1))[:, 0]
+    assert np.allclose(ana, num, rtol=1e-7, atol=1e-9)
+
+
+def test_fc1_backward_equals_autograd_of_the_moe_layer():
+    """The whole expert (FC1, SwiGLU, FC2, gate weight) for the retained pairs,
+    differentiated by autograd, gives the FC1 weight gradient, the token input
+    gradient (summed over the token's pairs) and the FC2 weight gradient of the
+    oracle's path; dropped pairs contribute nothing."""
+    import torch
+
+    T, k, E, h, I = 10, 2, 3, 6, 4
+    rng = np.random.default_rng(42)
+    g, phi_unused, W2, alpha, idx = _tiny(T=T, k=k, E=E, h=h, I=I, seed=43)
+    x_bits = f32_to_bf16_bits(rng.standard_normal((T, h)).astype(np.float32))
+    W1_bits = f32_to_bf16_bits((rng.standard_normal((E, 2 * I, h)) * 0.3).astype(np.float32))
+    x, W1 = O.bf16_to_f64(x_bits), O.bf16_to_f64(W1_bits)
+    e_u = idx.reshape(-1)
+    N = T * k
+    ab = np.stack([W1[e_u[u]] @ x[u // k] for u in range(N)])
+    for rho in (Fraction(1), Fraction(1, 2)):
+        st = O.route_stats(np.zeros((T, E), np.float32), idx, E, cf=Fraction(4), rho=rho)
+        R = O.score(g, f32_to_bf16_bits(O.swiglu_forward(ab).astype(np.float32)), alpha, k)
+        so, ids = O.select(R, idx, E, st["quota"])
+        dphi = O.grouped_dgrad(g, W2, alpha, so, ids, E, k)
+        rows = np.concatenate([dphi[e] for e in range(E)], axis=0)
+        dW1, dx_rows = O.fc1_backward(x, ab, W1, rows, so, ids, E, k)
+        dx = O.combine_pairs(dx_rows, ids, T, k)
+        # autograd of sum_t g_t . sum_{retained u of t} alpha_u W2_e silu(a_u) * b_u, [a_u; b_u] = W1_e x_t
+        tx = torch.tensor(x, requires_grad=True)
+        tW1 = torch.tensor(W1, requires_grad=True)
+        tW2 = torch.tensor(O.bf16_to_f64(W2), requires_grad=True)
+        tg = torch.tensor(O.bf16_to_f64(g))
+        loss = torch.zeros((), dtype=torch.float64)
+        for u in ids.tolist():
+            t, e = u // k, int(e_u[u])
+            abu = tW1[e] @ tx[t]
+            phiu = torch.nn.functional.silu(abu[:I]) * abu[I:]
+            loss = loss + float(alpha[u]) * (tg[t] @ (tW2[e] @ phiu))
+        loss.backward()
+        for e in range(E):
+            assert np.allclose(dW1[e], tW1.grad[e].numpy(), rtol=1e-10, atol=1e-12)
+        assert np.allclose(dx, tx.grad.numpy(), rtol=1e-10, atol=1e-12)
+        kept = np.zeros(N, dtype=bool)
+        kept[ids] = True
+        if rho == 1:
+            assert kept.all()
+        else:
+            assert not kept.all()
+
+
+def test_combine_pairs_hand_case():
+    rows = np.array([[1.0, 2.0], [10.0, 20.0], [100.0, 200.0]])
+    out = O.combine_pairs(rows, [0, 1, 5], T=4, k=2)
+    assert out.tolist() == [[11.0, 22.0], [0.0, 0.0], [100.0, 200.0], [0.0, 0.0]]
