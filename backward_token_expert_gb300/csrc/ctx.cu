@@ -10,6 +10,7 @@ namespace lrm {
 size_t route_stats_workspace_bytes(const lrm_dims& d);
 size_t select_workspace_bytes(const lrm_dims& d);
 size_t zero_dropped_workspace_bytes(const lrm_dims& d);
+size_t combine_workspace_bytes(const lrm_dims& d);
 }  // namespace lrm
 
 namespace {
@@ -107,6 +108,7 @@ lrm_status lrm_workspace_size(const lrm_ctx* ctx, lrm_op op, lrm_dims dims, size
     case LRM_OP_ROUTE_STATS: *bytes = route_stats_workspace_bytes(dims); return LRM_OK;
     case LRM_OP_SELECT: *bytes = select_workspace_bytes(dims); return LRM_OK;
     case LRM_OP_ZERO_DROPPED: *bytes = zero_dropped_workspace_bytes(dims); return LRM_OK;
+    case LRM_OP_COMBINE: *bytes = combine_workspace_bytes(dims); return LRM_OK;
   }
   return LRM_ERR_INVALID_ARG;
 }

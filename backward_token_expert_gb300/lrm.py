@@ -34,6 +34,7 @@ STATUS_NAMES = [
 LRM_OP_ROUTE_STATS = 0
 LRM_OP_SELECT = 1
 LRM_OP_ZERO_DROPPED = 2
+LRM_OP_COMBINE = 3
 
 # every entry point declared in include/lrm.h
 EXPORTED = (
@@ -57,6 +58,8 @@ EXPORTED = (
     "lrm_score_metric",
     "lrm_grouped_dgrad_scatter",
     "lrm_zero_dropped_rows",
+    "lrm_swiglu_backward",
+    "lrm_combine_rows",
 )
 
 # selection metrics of lrm_score_metric (the ablation of LRMoE sec. 4.7, Table 2)
@@ -134,6 +137,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "lrm_score_metric": ([P, i32, P, P, P, Dims, ctypes.c_uint64, P, P], st),
         "lrm_grouped_dgrad_scatter": ([P, P, P, P, P, Dims, i32, P, P], st),
         "lrm_zero_dropped_rows": ([P, P, P, Dims, i32, P, P, ctypes.c_size_t, P], st),
+        "lrm_swiglu_backward": ([P, P, P, P, Dims, i32, P, P], st),
+        "lrm_combine_rows": ([P, P, P, P, Dims, i32, i32, P, P, ctypes.c_size_t, P], st),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -251,6 +256,18 @@ def lrm_zero_dropped_rows(ctx, sel_offsets, sel_ids, dims: Dims, max_rows: int, 
     _check(load_library().lrm_zero_dropped_rows(ctx, _ptr(sel_offsets), _ptr(sel_ids), dims, int(max_rows),
                                                 _ptr(rows), _ptr(ws), int(ws_bytes), _stream(stream)),
            "lrm_zero_dropped_rows")
+
+
+def lrm_swiglu_backward(ctx, dphi_c, ab_c, sel_offsets, dims: Dims, max_rows: int, dh1, stream=None) -> None:
+    _check(load_library().lrm_swiglu_backward(ctx, _ptr(dphi_c), _ptr(ab_c), _ptr(sel_offsets), dims,
+                                              int(max_rows), _ptr(dh1), _stream(stream)), "lrm_swiglu_backward")
+
+
+def lrm_combine_rows(ctx, rows, sel_offsets, sel_ids, dims: Dims, max_rows: int, width: int, out, ws, ws_bytes: int,
+                     stream=None) -> None:
+    _check(load_library().lrm_combine_rows(ctx, _ptr(rows), _ptr(sel_offsets), _ptr(sel_ids), dims, int(max_rows),
+                                           int(width), _ptr(out), _ptr(ws), int(ws_bytes), _stream(stream)),
+           "lrm_combine_rows")
 
 
 def lrm_select(ctx, score, offsets, bucket, quota, dims: Dims, max_rows: int, sel_offsets, sel_ids, ws=None,

@@ -42,6 +42,20 @@ def max_retained_rows(T: int, E: int, k: int, cf: Fraction, rho: Fraction) -> in
 
 
 @dataclasses.dataclass
+class Fc1Buffers:
+    """Device buffers of the FC1 side (allocated on first use)."""
+
+    ones: torch.Tensor  # [N] fp32: unit gate weights for compacting the FC1 inputs
+    xc: torch.Tensor  # [rows, h] bf16: compacted expert inputs
+    abc: torch.Tensor  # [rows, 2I] bf16: compacted saved FC1 outputs
+    dh1: torch.Tensor  # [rows, 2I] bf16: FC1 output gradient
+    dxc: torch.Tensor  # [rows, h] bf16: FC1 input gradient per retained row
+    dW1: torch.Tensor  # [E, 2I, h] fp32
+    dx: torch.Tensor  # [T, h] bf16: input gradient of every token
+    ws: torch.Tensor  # pair -> row map of lrm_combine_rows
+
+
+@dataclasses.dataclass
 class Buffers:
     counts: torch.Tensor
     offsets: torch.Tensor
@@ -158,6 +172,41 @@ class Recalibration:
                 self._ws_zero = torch.empty(max(nbytes, 4), dtype=torch.uint8, device=self.buf.dW.device)
             L.lrm_zero_dropped_rows(self.ctx, b.sel_offsets, b.sel_ids, self.dims, self.max_rows, dphi_rows,
                                     self._ws_zero, self._ws_zero.numel(), stream)
+
+    def fc1_backward(self, x, ab, W1, stream=None):
+        """The FC1 side of the expert backward on the retained pairs (SwiGLU
+        read), after the FC2 steps: the compacted FC1 inputs, dh1 from the FC2
+        input gradient, the FC1 input gradient of every retained row, the FC1
+        weight gradient and the input gradient of every token.  x [T, h] and
+        ab [N, 2I] bf16 (expert inputs, saved [a | b]), W1 [E, 2I, h] bf16.
+        Results: self.fc1.dW1 [E, 2I, h] fp32 and self.fc1.dx [T, h] bf16."""
+        f = self._fc1_buffers()
+        b = self.buf
+        T, E, k, h, I = self.dims.T, self.dims.E, self.dims.k, self.dims.h, self.dims.I
+        d_in = L.Dims(T, E, k, h, 2 * I)  # compact: token rows of width h, pair rows of width 2I
+        d_fc1 = L.Dims(T, E, k, 2 * I, h)  # the FC2 kernels with K = 2I and output width h
+        L.lrm_compact(self.ctx, x, ab, f.ones, b.sel_offsets, b.sel_ids, d_in, self.max_rows, f.xc, f.abc, None,
+                      stream)
+        L.lrm_swiglu_backward(self.ctx, b.dphi_c, f.abc, b.sel_offsets, self.dims, self.max_rows, f.dh1, stream)
+        L.lrm_grouped_dgrad(self.ctx, f.dh1, W1, b.sel_offsets, d_fc1, self.max_rows, f.dxc, stream)
+        L.lrm_grouped_wgrad(self.ctx, f.dh1, f.xc, b.sel_offsets, d_fc1, self.max_rows, 0, f.dW1, stream)
+        L.lrm_combine_rows(self.ctx, f.dxc, b.sel_offsets, b.sel_ids, self.dims, self.max_rows, h, f.dx, f.ws,
+                           f.ws.numel(), stream)
+
+    def _fc1_buffers(self):
+        if getattr(self, "fc1", None) is None:
+            T, E, k, h, I = self.dims.T, self.dims.E, self.dims.k, self.dims.h, self.dims.I
+            dev = self.buf.dW.device
+            bf = dict(dtype=torch.bfloat16, device=dev)
+            rows = max(self.max_rows, 1)
+            ws = L.lrm_workspace_size(self.ctx, L.LRM_OP_COMBINE, self.dims)
+            self.fc1 = Fc1Buffers(
+                ones=torch.ones(T * k, dtype=torch.float32, device=dev),
+                xc=torch.empty(rows, h, **bf), abc=torch.empty(rows, 2 * I, **bf),
+                dh1=torch.empty(rows, 2 * I, **bf), dxc=torch.empty(rows, h, **bf),
+                dW1=torch.empty(E, 2 * I, h, dtype=torch.float32, device=dev), dx=torch.empty(T, h, **bf),
+                ws=torch.empty(max(ws, 4), dtype=torch.uint8, device=dev))
+        return self.fc1
 
     def wgrad(self, stream=None, accumulate=0):
         b = self.buf

@@ -72,7 +72,12 @@ typedef enum lrm_status {
 } lrm_status;
 
 /* Operations that take a workspace, for lrm_workspace_size. */
-typedef enum lrm_op { LRM_OP_ROUTE_STATS = 0, LRM_OP_SELECT = 1, LRM_OP_ZERO_DROPPED = 2 } lrm_op;
+typedef enum lrm_op {
+  LRM_OP_ROUTE_STATS = 0,
+  LRM_OP_SELECT = 1,
+  LRM_OP_ZERO_DROPPED = 2,
+  LRM_OP_COMBINE = 3
+} lrm_op;
 
 /* Layer sizes.  Limits: 1 <= E <= 1024, 1 <= k <= 32, k <= E, N = T*k < 2^31,
  * h and I multiples of 8 in [8, 65536]. */
@@ -244,6 +249,38 @@ LRM_API lrm_status lrm_grouped_dgrad_scatter(lrm_ctx* ctx, const uint16_t* delta
 LRM_API lrm_status lrm_zero_dropped_rows(lrm_ctx* ctx, const int32_t* sel_offsets, const int32_t* sel_ids,
                                  lrm_dims dims, int32_t max_rows, uint16_t* rows, void* ws, size_t ws_bytes,
                                  void* stream);
+
+/*
+ * FC1 side of the expert backward on the retained pairs (LRMoE sec. 3.4:
+ * compaction reduces the row dimension of all four expert-backward GEMMs).
+ * The activation is read as SwiGLU: FC1 gives [a | b] (gate, up; width 2I)
+ * per pair and phi = silu(a) * b, silu(a) = a / (1 + exp(-a)).  The FC1 GEMMs
+ * are lrm_grouped_dgrad / lrm_grouped_wgrad with the dimensions relabelled:
+ *   compacted FC1 inputs:   lrm_compact(g = x [T, h], phi = ab [N, 2I], alpha = 1,
+ *                           dims with I -> 2I) gives Xc and ABc;
+ *   FC1 input gradient:     lrm_grouped_dgrad(delta_c = dh1, W = W1 [E, 2I, h],
+ *                           dims with h -> 2I, I -> h) gives dXc [rows, h];
+ *   FC1 weight gradient:    lrm_grouped_wgrad(delta_c = dh1, phi_c = Xc,
+ *                           dims with h -> 2I, I -> h) gives dW1 [E, 2I, h].
+ *
+ * lrm_swiglu_backward: dh1[r] = [dphi_c[r] * b * silu'(a) | dphi_c[r] * silu(a)]
+ * for the compacted rows r < sel_offsets[E] (clamped to max_rows), [a | b] =
+ * ab_c[r]; fp32 math, bf16 (round to nearest even) out.
+ *   dphi_c [rows, I] bf16, ab_c [rows, 2I] bf16, dh1 [rows, 2I] bf16
+ *
+ * lrm_combine_rows: the input gradient of every token: out[t] = bf16(sum of
+ * rows[r] over the retained pairs u = sel_ids[r] of token t = u div k), zeros
+ * for tokens without a retained pair (the inverse mapping followed by the MoE
+ * combine over the token's k experts).  rows [max_rows, width] bf16 (the
+ * compacted order), out [T, width] bf16, width a multiple of 8.  ws: N int32
+ * (lrm_workspace_size with LRM_OP_COMBINE).
+ */
+LRM_API lrm_status lrm_swiglu_backward(lrm_ctx* ctx, const uint16_t* dphi_c, const uint16_t* ab_c,
+                               const int32_t* sel_offsets, lrm_dims dims, int32_t max_rows, uint16_t* dh1,
+                               void* stream);
+LRM_API lrm_status lrm_combine_rows(lrm_ctx* ctx, const uint16_t* rows, const int32_t* sel_offsets,
+                            const int32_t* sel_ids, lrm_dims dims, int32_t max_rows, int32_t width, uint16_t* out,
+                            void* ws, size_t ws_bytes, void* stream);
 
 /*
  * Step 5b - grouped FC2 weight gradient, variable K, no padding (LRMoE

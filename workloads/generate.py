@@ -199,3 +199,28 @@ def generate(w: Workload | str, parts=("g", "phi", "W")) -> Inputs:
         W = _fill_bf16(ss[5], w.E * w.h * w.I,
                        lambda v, s, e: v * np.float32(0.02)).reshape(w.E, w.h, w.I)
     return Inputs(w, logits, expert_idx, alpha, g, phi, W, bias)
+
+
+@dataclasses.dataclass
+class Fc1Inputs:
+    """The saved state of the FC1 side of the expert backward (SwiGLU read):
+    the expert input of every token, the saved FC1 output [a | b] (gate, up)
+    of every pair, and the FC1 weights.  They are drawn independently of the
+    FC2 tensors of ``generate`` (the backward takes them as given)."""
+
+    x: np.ndarray  # [T, h] bf16 bits: expert input of token t
+    ab: np.ndarray  # [T*k, 2I] bf16 bits: saved FC1 output [a | b] of pair u
+    W1: np.ndarray  # [E, 2I, h] bf16 bits: FC1 weight (gate rows first)
+
+
+def fc1_inputs(w: Workload | str) -> Fc1Inputs:
+    """x ~ N(0, 1), [a | b] ~ N(0, 1), W1 ~ N(0, 0.02^2), bf16; from the child
+    seeds 6, 7, 8 of the workload's SeedSequence (children 0-5 feed
+    ``generate``, so its tensors do not change)."""
+    if isinstance(w, str):
+        w = get_workload(w)
+    ss = np.random.SeedSequence(w.seed).spawn(9)
+    x = _fill_bf16(ss[6], w.T * w.h).reshape(w.T, w.h)
+    ab = _fill_bf16(ss[7], w.N * 2 * w.I).reshape(w.N, 2 * w.I)
+    W1 = _fill_bf16(ss[8], w.E * 2 * w.I * w.h, lambda v, s, e: v * np.float32(0.02)).reshape(w.E, 2 * w.I, w.h)
+    return Fc1Inputs(x, ab, W1)
