@@ -1,7 +1,7 @@
 // Step 1 of the path: routing statistics, capacity, drop rate and retention
 // quotas ("Expert Parallel Math Deep": importance P_e, load f_e, the
 // auxiliary loss E * sum f_e P_e, capacity C = CF * T k / E and the drop
-// rate; LRMoE sec. 3.1 and Alg. 1 line 1: routed counts n_e and quotas
+// rate; LRMoE sec. 3.1 and Alg. 1: routed counts n_e and quotas
 // 0 <= Q_e <= n_e), plus the stable expert bucket and prefix offsets that
 // selection and compaction consume (LRMoE sec. 3.3).
 //

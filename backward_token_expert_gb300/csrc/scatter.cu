@@ -1,4 +1,4 @@
-// The inverse mapping of LRMoE (sec. 1 and 3.3; Alg. 1 line 19,
+// The inverse mapping of LRMoE (sec. 1 and 3.3; Alg. 1,
 // ScatterWithZeros; sec. 3.4: the retained results go back to their original
 // positions and zeros are restored before the next dense-layer boundary).
 // lrm_grouped_dgrad_scatter writes every retained row of the input gradient

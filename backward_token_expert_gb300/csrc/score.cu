@@ -1,5 +1,5 @@
 // Step 2 of the path: the Load Recalibration Metric of LRMoE (sec. 3.2,
-// Prop. 3.1 eq. (3); Alg. 1 line 13; appendix 7.1 eq. (11)-(12)):
+// Prop. 3.1 eq. (3); Alg. 1; appendix 7.1 eq. (11)-(12)):
 //   R_u = alpha_u^2 * ||g_t||^2 * ||phi_u||^2 for every routed pair u = t*k + j.
 // The squared norm of g_t is computed once per token and shared by its k
 // pairs.  HBM-bound: every byte of g and phi is read exactly once.

@@ -1,5 +1,5 @@
 // Step 3 of the path: per-expert TopK within the quota (LRMoE sec. 3.2 and
-// 3.3, Alg. 1 line 14; appendix 7.2 Prop. 7.1: for fixed per-expert quotas,
+// 3.3, Alg. 1; appendix 7.2 Prop. 7.1: for fixed per-expert quotas,
 // keeping the largest scores of every expert is optimal, and ties only
 // change which of the equal boundary scores are kept).
 //

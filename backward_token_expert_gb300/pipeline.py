@@ -8,7 +8,7 @@ synchronisation in between:
     lrm_route_stats -> lrm_score -> lrm_select -> lrm_compact
                     -> lrm_grouped_dgrad -> lrm_grouped_wgrad
 
-(LRMoE Alg. 1 lines 1 and 13-17; the input-gradient product runs before the
+(LRMoE Alg. 1; the input-gradient product runs before the
 weight-gradient product, the order TopoEP sec. 3.3 schedules them in).
 """
 

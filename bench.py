@@ -341,6 +341,7 @@ def run_ours(args, rank, world, local):
         if not args.no_comparator:
             result["comparator"] = comparator(rec, d, w, retained, pk)
             result["inverse_mapping"] = inverse_mapping(rec, d, w, retained, pk)
+            result["fc1_backward"] = fc1_backward(rec, w, retained, pk)
         if not args.no_cpu_baseline:
             result["cpu_baseline"] = cpu_baseline(inp, tokens=args.ref_tokens or 8192)
     if not args.no_e2e:
@@ -387,6 +388,71 @@ def inverse_mapping(rec, d, w, retained, pk, iters=20):
     if flags:
         raise RuntimeError(f"device status flags {flags:#x} in the inverse mapping")
     return out
+
+
+def fc1_backward(rec, w, retained, pk, iters=20):
+    """The FC1 side of the expert backward on the retained pairs (SwiGLU read),
+    after the timed FC2 steps have left their compacted input gradient: each of
+    its five library calls timed alone, with its roofline from the algorithmic
+    bytes (and flop) per launch."""
+    import torch
+
+    from backward_token_expert_gb300 import lrm as L
+    from workloads import fc1_inputs
+
+    f1 = fc1_inputs(w)
+
+    def dev(bits):
+        return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).cuda()
+
+    x, ab, W1 = dev(f1.x), dev(f1.ab), dev(f1.W1)
+    del f1
+    rec.fc1_backward(x, ab, W1)  # allocates the FC1 buffers
+    f, b, ctx, mr = rec.fc1, rec.buf, rec.ctx, rec.max_rows
+    T, E, k, h, I = w.T, w.E, w.k, w.h, w.I
+    d_in, d_fc1 = L.Dims(T, E, k, h, 2 * I), L.Dims(T, E, k, 2 * I, h)
+    act = int((b.sel_offsets[1:] > b.sel_offsets[:-1]).sum().item())
+    gemm_flop = 2 * retained * 2 * I * h
+    calls = {
+        "compact": (lambda: L.lrm_compact(ctx, x, ab, f.ones, b.sel_offsets, b.sel_ids, d_in, mr, f.xc, f.abc, None),
+                    (retained * (4 * h + 8 * I + 8), 0)),
+        "swiglu_backward": (lambda: L.lrm_swiglu_backward(ctx, b.dphi_c, f.abc, b.sel_offsets, rec.dims, mr, f.dh1),
+                            (retained * 10 * I, 0)),
+        "dgrad": (lambda: L.lrm_grouped_dgrad(ctx, f.dh1, W1, b.sel_offsets, d_fc1, mr, f.dxc),
+                  (retained * 2 * (2 * I + h) + act * 4 * I * h, gemm_flop)),
+        "wgrad": (lambda: L.lrm_grouped_wgrad(ctx, f.dh1, f.xc, b.sel_offsets, d_fc1, mr, 0, f.dW1),
+                  (retained * 2 * (2 * I + h) + E * 8 * I * h, gemm_flop)),
+        "combine": (lambda: L.lrm_combine_rows(ctx, f.dxc, b.sel_offsets, b.sel_ids, rec.dims, mr, h, f.dx, f.ws,
+                                               f.ws.numel()),
+                    (8 * w.N + 8 * retained + retained * 2 * h + T * 2 * h, 0)),
+    }
+    s = torch.cuda.current_stream()
+    out = {}
+    for name, (fn, (nbytes, flop)) in calls.items():
+        for _ in range(3):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(iters):
+            fn()
+        e1.record(s)
+        e1.synchronize()
+        ms = e0.elapsed_time(e1) / iters
+        out[name] = dict(ms=round(ms, 5), **roofline_entry(nbytes, flop, ms, pk, sustained=False))
+    for _ in range(3):
+        rec.fc1_backward(x, ab, W1)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(iters):
+        rec.fc1_backward(x, ab, W1)
+    e1.record(s)
+    e1.synchronize()
+    total = e0.elapsed_time(e1) / iters
+    flags = rec.device_status()
+    if flags:
+        raise RuntimeError(f"device status flags {flags:#x} in the FC1 backward")
+    return {"what": "compact x and [a|b], SwiGLU backward, FC1 dgrad and wgrad (K = 2I), combine per token",
+            "ms": round(total, 5), "pairs_per_s": round(retained / (total * 1e-3), 1), "kernels": out}
 
 
 def comparator(rec, d, w, retained, pk, iters=20):

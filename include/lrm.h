@@ -3,9 +3,8 @@
  * backward recalibration of one MoE layer's FC2 (down) projection.
  *
  * Source: "LRMoE: Demand-Side Load Re-Calibration for Efficient MoE Training
- * on Memory-Constrained Nodes" (Hu et al.), sec. 3.1-3.4, Alg. 1 lines 1 and
- * 13-17, Fig. 4, appendix 7.1-7.2; routing statistics from "Expert Parallel
- * Math Deep" (sections on routing as an expectation over a batch, the
+ * on Memory-Constrained Nodes" (Hu et al.), sec. 3.1-3.4, Alg. 1, Fig. 4,
+ * appendix 7.1-7.2; routing statistics from "Expert Parallel Math Deep" (sections on routing as an expectation over a batch, the
  * load-balancing auxiliary loss, and capacity / drop rate).
  *
  * The path, in call order on one stream, with no host synchronisation:
@@ -125,7 +124,7 @@ LRM_API lrm_status lrm_workspace_size(const lrm_ctx* ctx, lrm_op op, lrm_dims di
  * Step 1 - routing statistics and retention quotas.
  * "Expert Parallel Math Deep": P_e = (1/T) sum_t softmax(logits_t)_e over all
  * E experts, f_e = n_e / N, aux = E sum f_e P_e, C = CF N / E,
- * dropped = sum max(0, n_e - C).  LRMoE sec. 3.1 / Alg. 1 line 1: routed
+ * dropped = sum max(0, n_e - C).  LRMoE sec. 3.1 / Alg. 1: routed
  * counts n_e and quotas K_e (here Q_e) with 0 <= Q_e <= n_e; the quota rule is
  * Q_e = ceil(rho * min(n_e, C)); CF = cf_num/cf_den and rho = rho_num/rho_den
  * are exact rationals (C is the floor).
@@ -148,7 +147,7 @@ LRM_API lrm_status lrm_route_stats(lrm_ctx* ctx, const float* logits, const int3
 
 /*
  * Step 2 - the Load Recalibration Metric (LRMoE sec. 3.2 Prop. 3.1 eq. (3);
- * Alg. 1 line 13): score[u] = alpha[u]^2 * ||g_t||^2 * ||phi_u||^2, the
+ * Alg. 1): score[u] = alpha[u]^2 * ||g_t||^2 * ||phi_u||^2, the
  * squared Frobenius norm of the rank-one gradient contribution
  * (alpha_u g_t) phi_u^T, in fp32.
  *   g     [T, h]    bf16  gradient at the expert output, before alpha
@@ -183,7 +182,7 @@ LRM_API lrm_status lrm_score_metric(lrm_ctx* ctx, int32_t metric, const uint16_t
                             const float* alpha, lrm_dims dims, uint64_t seed, float* score, void* stream);
 
 /*
- * Step 3 - per-expert TopK within the quota (LRMoE sec. 3.2, Alg. 1 line 14,
+ * Step 3 - per-expert TopK within the quota (LRMoE sec. 3.2, Alg. 1,
  * appendix 7.2 Prop. 7.1): for every expert e keep the quota[e] pairs of
  * bucket[offsets[e] .. offsets[e+1]) with the largest score; equal scores go
  * to the lower pair index.  Retained ids are written expert-major, ascending
@@ -227,7 +226,7 @@ LRM_API lrm_status lrm_grouped_dgrad(lrm_ctx* ctx, const uint16_t* delta_c, cons
                              uint16_t* dphi_c, void* stream);
 
 /*
- * The inverse mapping (LRMoE sec. 1 and 3.3; Alg. 1 line 19, ScatterWithZeros;
+ * The inverse mapping (LRMoE sec. 1 and 3.3; Alg. 1, ScatterWithZeros;
  * sec. 3.4: retained results go back to their original positions, zeros are
  * restored before the next dense-layer boundary), in two calls:
  *

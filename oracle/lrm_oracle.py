@@ -11,7 +11,7 @@ Sources (cited by page title and the section / equation / figure):
   Memory-Constrained Nodes" (Hu et al.), called LRMoE below:
   sec. 3.1 (quotas K_e with rho = sum K_e / N; compaction in a consistent pair
   order with counts and prefix offsets), sec. 3.2 Prop. 3.1 eq. (1)-(3) (the
-  Load Recalibration Metric), sec. 3.3 Alg. 1 lines 13-17 (score, per-expert
+  Load Recalibration Metric), sec. 3.3 Alg. 1 (score, per-expert
   TopK, compaction, packed expert backward), Fig. 4 and sec. 3.4 (variable-M
   grouped GEMMs without padding; equivalence with zero-masking), appendix 7.1
   eq. (4)-(12) (FC2 shapes, weighted cotangent delta_u = alpha_u g_t, rank-one
@@ -128,7 +128,7 @@ def _ceil_div(a, b):
 def route_stats(logits, expert_idx, E: int, cf=Fraction(5, 4), rho=Fraction(3, 4), quota=None):
     """Per-expert routing statistics, capacity, drop rate and retention quotas.
 
-    * n_e = number of routed pairs on expert e (LRMoE Alg. 1 line 1);
+    * n_e = number of routed pairs on expert e (LRMoE Alg. 1);
     * P_e = mean over tokens of the full softmax, f_e = n_e / (T k), and
       aux = E * sum_e f_e P_e (EPM);
     * C = CF * T k / E (floor of the exact rational), dropped_e =
@@ -270,7 +270,7 @@ def score_metric(metric: int, g_bits, phi_bits, alpha, k: int, seed: int = 0, n_
 
 
 # ---------------------------------------------------------------------------
-# step 3: per-expert TopK within the quota (LRMoE sec. 3.2, Alg. 1 line 14, Prop. 7.1)
+# step 3: per-expert TopK within the quota (LRMoE sec. 3.2, Alg. 1, Prop. 7.1)
 
 
 def select(R, expert_of_pair, E: int, quota):
@@ -341,7 +341,7 @@ def compact_padded(delta_c, phi_c, sel_offsets, E: int, C: int):
 
 
 # ---------------------------------------------------------------------------
-# step 5: packed expert backward of FC2 (LRMoE Alg. 1 line 17; app. 7.1 eq. (6)-(9))
+# step 5: packed expert backward of FC2 (LRMoE Alg. 1; app. 7.1 eq. (6)-(9))
 
 
 def grouped_wgrad(g_bits, phi_bits, alpha, sel_offsets, sel_ids, E: int, k: int, experts=None):
@@ -382,7 +382,7 @@ def grouped_dgrad(g_bits, W_bits, alpha, sel_offsets, sel_ids, E: int, k: int, e
 
 
 def scatter_with_zeros(rows, sel_ids, N: int) -> np.ndarray:
-    """The inverse mapping of LRMoE (sec. 1 and 3.3; Alg. 1 line 19,
+    """The inverse mapping of LRMoE (sec. 1 and 3.3; Alg. 1,
     ScatterWithZeros; sec. 3.4: retained results go back to their original
     positions and zeros are restored before the next dense-layer boundary):
     row r of `rows` (the r-th retained pair in the compacted order) goes to

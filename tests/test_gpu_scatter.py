@@ -1,4 +1,4 @@
-"""The inverse mapping (LRMoE Alg. 1 line 19, ScatterWithZeros; sec. 3.4) on the
+"""The inverse mapping (LRMoE Alg. 1, ScatterWithZeros; sec. 3.4) on the
 GPU: the scattered input gradient holds, at row u of every retained pair, the
 same bits as the compacted dgrad output, and exact zeros at every other row;
 against the oracle it is the scattered fp64 gradient within the GEMM bound."""
