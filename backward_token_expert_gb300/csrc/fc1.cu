@@ -80,7 +80,26 @@ __global__ void __launch_bounds__(F1_THREADS) map_kernel(const int32_t* __restri
   }
 }
 
-// out[t] = bf16(sum over retained pairs u of t of rows[pos[u]]), one warp per token
+__device__ __forceinline__ void add8(float (&acc)[8], const uint4& x) {
+  acc[0] += bf16_lo(x.x);
+  acc[1] += bf16_hi(x.x);
+  acc[2] += bf16_lo(x.y);
+  acc[3] += bf16_hi(x.y);
+  acc[4] += bf16_lo(x.z);
+  acc[5] += bf16_hi(x.z);
+  acc[6] += bf16_lo(x.w);
+  acc[7] += bf16_hi(x.w);
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&acc)[8]) {
+  return make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
+                    pack_bf16x2(acc[6], acc[7]));
+}
+
+// out[t] = bf16(sum over the retained pairs u of t, in slot order, of
+// rows[pos[u]]); one warp per token.  The warp first moves the row indices of
+// its retained pairs to its low lanes (n of them), then each lane sums two
+// 16-byte chunks of the row at a time with up to eight loads in flight.
 __global__ void __launch_bounds__(F1_THREADS) combine_kernel(const uint4* __restrict__ rows,
                                                              const int32_t* __restrict__ pos, int T, int k, int wv,
                                                              uint4* __restrict__ out) {
@@ -88,25 +107,46 @@ __global__ void __launch_bounds__(F1_THREADS) combine_kernel(const uint4* __rest
   const int warps_total = gridDim.x * F1_WARPS;
   for (int t = blockIdx.x * F1_WARPS + (threadIdx.x >> 5); t < T; t += warps_total) {
     const int my = lane < k ? __ldg(pos + static_cast<size_t>(t) * k + lane) : -1;
-    for (int v0 = 0; v0 < wv; v0 += 32) {  // every lane runs every step (the shuffles below)
-      const int v = v0 + lane;
-      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      for (int j = 0; j < k; ++j) {
-        const int r = __shfl_sync(0xffffffffu, my, j);
-        if (r < 0 || v >= wv) continue;
-        const uint4 x = ld_stream(rows + static_cast<size_t>(r) * wv + v);
-        acc[0] += bf16_lo(x.x);
-        acc[1] += bf16_hi(x.x);
-        acc[2] += bf16_lo(x.y);
-        acc[3] += bf16_hi(x.y);
-        acc[4] += bf16_lo(x.z);
-        acc[5] += bf16_hi(x.z);
-        acc[6] += bf16_lo(x.w);
-        acc[7] += bf16_hi(x.w);
+    const unsigned kept = __ballot_sync(0xffffffffu, my >= 0);
+    const int n = __popc(kept);
+    const unsigned src = __fns(kept, 0, lane + 1);  // slot of the (lane+1)-th kept pair
+    const int row = __shfl_sync(0xffffffffu, my, static_cast<int>(src & 31u));
+    uint4* orow = out + static_cast<size_t>(t) * wv;
+    for (int v0 = 0; v0 < wv; v0 += 64) {  // uniform trip count: the shuffles below need every lane
+      const int va = v0 + lane, vb = va + 32;
+      const bool ia = va < wv, ib = vb < wv;
+      float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      float b[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      int j = 0;
+      for (; j + 4 <= n; j += 4) {
+        const int r0 = __shfl_sync(0xffffffffu, row, j), r1 = __shfl_sync(0xffffffffu, row, j + 1);
+        const int r2 = __shfl_sync(0xffffffffu, row, j + 2), r3 = __shfl_sync(0xffffffffu, row, j + 3);
+        const uint4* p0 = rows + static_cast<size_t>(r0) * wv;
+        const uint4* p1 = rows + static_cast<size_t>(r1) * wv;
+        const uint4* p2 = rows + static_cast<size_t>(r2) * wv;
+        const uint4* p3 = rows + static_cast<size_t>(r3) * wv;
+        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+        const uint4 xa0 = ia ? ld_stream(p0 + va) : z, xa1 = ia ? ld_stream(p1 + va) : z;
+        const uint4 xa2 = ia ? ld_stream(p2 + va) : z, xa3 = ia ? ld_stream(p3 + va) : z;
+        const uint4 xb0 = ib ? ld_stream(p0 + vb) : z, xb1 = ib ? ld_stream(p1 + vb) : z;
+        const uint4 xb2 = ib ? ld_stream(p2 + vb) : z, xb3 = ib ? ld_stream(p3 + vb) : z;
+        add8(a, xa0);
+        add8(a, xa1);
+        add8(a, xa2);
+        add8(a, xa3);
+        add8(b, xb0);
+        add8(b, xb1);
+        add8(b, xb2);
+        add8(b, xb3);
       }
-      if (v < wv)
-        out[static_cast<size_t>(t) * wv + v] = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
-                                                          pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+      for (; j < n; ++j) {
+        const int r = __shfl_sync(0xffffffffu, row, j);
+        const uint4* pr = rows + static_cast<size_t>(r) * wv;
+        if (ia) add8(a, ld_stream(pr + va));
+        if (ib) add8(b, ld_stream(pr + vb));
+      }
+      if (ia) orow[va] = pack8(a);
+      if (ib) orow[vb] = pack8(b);
     }
   }
 }

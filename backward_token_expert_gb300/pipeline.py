@@ -250,3 +250,85 @@ def to_device_inputs(inp, device="cuda"):
         phi=bf(inp.phi),
         W=bf(inp.W),
     )
+
+
+INPUT_NAMES = ("logits", "expert_idx", "g", "phi", "alpha", "W")
+OUTPUT_NAMES = ("dW", "dphi_c", "sel_offsets", "sel_ids", "summary")
+
+
+class HostPipeline:
+    """The path over a sequence of host-resident layer batches, with the
+    host->device copies of one batch and the device->host copies of the one
+    before it running on their own streams while a third computes.
+
+    Two slots (each a ``Recalibration`` with its own device inputs and
+    outputs) alternate; events order every reuse: a slot's inputs are not
+    overwritten before its last compute has read them, and its outputs are
+    not recomputed before they were copied out.  ``submit`` only enqueues;
+    the caller keeps each host buffer untouched until ``synchronize`` (or
+    until two later submits have completed).  Host buffers should be pinned
+    for the copies to run asynchronously.
+    """
+
+    def __init__(self, T, E, k, h, I, cf=Fraction(5, 4), rho=Fraction(3, 4), device=0):
+        self.recs = [Recalibration(T, E, k, h, I, cf, rho, device=device) for _ in range(2)]
+        dev = self.recs[0].device
+        self.device = dev
+        N = int(T) * int(k)
+        bf = dict(dtype=torch.bfloat16, device=dev)
+        self.dev_in = [dict(logits=torch.empty(T, E, dtype=torch.float32, device=dev),
+                            expert_idx=torch.empty(T, k, dtype=torch.int32, device=dev),
+                            g=torch.empty(T, h, **bf), phi=torch.empty(N, I, **bf),
+                            alpha=torch.empty(N, dtype=torch.float32, device=dev), W=torch.empty(E, h, I, **bf))
+                       for _ in range(2)]
+        self.s_in, self.s_comp, self.s_out = (torch.cuda.Stream(dev) for _ in range(3))
+        self.ev_in, self.ev_comp, self.ev_out = ([torch.cuda.Event() for _ in range(2)] for _ in range(3))
+        self.submitted = 0
+
+    def submit(self, host_in: dict, host_out: dict) -> int:
+        """Enqueue one batch: copy `host_in` (the six inputs, by name) in, run
+        the path, copy the results into `host_out` (dW, dphi_c, sel_offsets,
+        sel_ids, summary).  Returns the slot used."""
+        s = self.submitted % 2
+        rec, din = self.recs[s], self.dev_in[s]
+        reuse = self.submitted >= 2
+        if reuse:
+            self.s_in.wait_event(self.ev_comp[s])
+        with torch.cuda.stream(self.s_in):
+            for name in INPUT_NAMES:
+                din[name].copy_(host_in[name], non_blocking=True)
+        self.ev_in[s].record(self.s_in)
+        self.s_comp.wait_event(self.ev_in[s])
+        if reuse:
+            self.s_comp.wait_event(self.ev_out[s])
+        rec.run(din["logits"], din["expert_idx"], din["g"], din["phi"], din["alpha"], din["W"], stream=self.s_comp)
+        self.ev_comp[s].record(self.s_comp)
+        self.s_out.wait_event(self.ev_comp[s])
+        b = rec.buf
+        with torch.cuda.stream(self.s_out):
+            for name in OUTPUT_NAMES:
+                host_out[name].copy_(getattr(b, name), non_blocking=True)
+        self.ev_out[s].record(self.s_out)
+        self.submitted += 1
+        return s
+
+    def host_outputs(self, pin: bool = True) -> dict:
+        """A set of host buffers shaped for ``submit``'s results."""
+        b = self.recs[0].buf
+        out = {name: torch.empty_like(getattr(b, name), device="cpu") for name in OUTPUT_NAMES}
+        return {k2: v.pin_memory() for k2, v in out.items()} if pin else out
+
+    def synchronize(self) -> None:
+        for st in (self.s_in, self.s_comp, self.s_out):
+            st.synchronize()
+
+    def device_status(self) -> int:
+        flags = 0
+        for rec in self.recs:
+            flags |= rec.device_status(self.s_comp)
+        self.s_comp.synchronize()
+        return flags
+
+    def close(self) -> None:
+        for rec in self.recs:
+            rec.close()

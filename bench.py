@@ -506,9 +506,14 @@ def comparator(rec, d, w, retained, pk, iters=20):
 
 
 def e2e(rec, inp, w, retained, iters, local):
-    """Same metric through the public API with host buffers: pinned host->device
-    copies of the step's inputs, the path, device->host copies of its results."""
+    """Same metric through the public API with host buffers: every step copies
+    its inputs from pinned host memory, runs the path and copies its results
+    back (HostPipeline: the copies of neighbouring steps overlap the compute
+    on their own streams)."""
     import torch
+
+    from backward_token_expert_gb300.pipeline import HostPipeline
+    from backward_token_expert_gb300.replicas import job_totals
 
     def pinned(a, dtype=None):
         t = torch.from_numpy(np.ascontiguousarray(a))
@@ -519,40 +524,32 @@ def e2e(rec, inp, w, retained, iters, local):
     h_in = dict(logits=pinned(inp.logits), expert_idx=pinned(inp.expert_idx), alpha=pinned(inp.alpha),
                 g=pinned(inp.g.view(np.int16), torch.bfloat16), phi=pinned(inp.phi.view(np.int16), torch.bfloat16),
                 W=pinned(inp.W.view(np.int16), torch.bfloat16))
-    dev = {k2: torch.empty_like(v, device=f"cuda:{local}") for k2, v in h_in.items()}
-    b = rec.buf
-    h_out = dict(dW=torch.empty_like(b.dW, device="cpu").pin_memory(),
-                 dphi_c=torch.empty_like(b.dphi_c, device="cpu").pin_memory(),
-                 sel_offsets=torch.empty_like(b.sel_offsets, device="cpu").pin_memory(),
-                 sel_ids=torch.empty_like(b.sel_ids, device="cpu").pin_memory(),
-                 summary=torch.empty_like(b.summary, device="cpu").pin_memory())
+    pipe = HostPipeline(w.T, w.E, w.k, w.h, w.I, w.cf, w.rho, device=local)
+    h_out = [pipe.host_outputs(), pipe.host_outputs()]
     h2d = sum(v.numel() * v.element_size() for v in h_in.values())
-    d2h = sum(v.numel() * v.element_size() for v in h_out.values())
-
-    def one():
-        for k2, v in h_in.items():
-            dev[k2].copy_(v, non_blocking=True)
-        rec.run(dev["logits"], dev["expert_idx"], dev["g"], dev["phi"], dev["alpha"], dev["W"])
-        h_out["dW"].copy_(b.dW, non_blocking=True)
-        h_out["dphi_c"].copy_(b.dphi_c, non_blocking=True)
-        h_out["sel_offsets"].copy_(b.sel_offsets, non_blocking=True)
-        h_out["sel_ids"].copy_(b.sel_ids, non_blocking=True)
-        h_out["summary"].copy_(b.summary, non_blocking=True)
-
-    from backward_token_expert_gb300.replicas import job_totals
-
-    for _ in range(2):
-        one()
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for _ in range(iters):
-        one()
-    torch.cuda.synchronize()
-    dt = time.perf_counter() - t0
+    d2h = sum(v.numel() * v.element_size() for v in h_out[0].values())
+    try:
+        for i in range(3):
+            pipe.submit(h_in, h_out[i % 2])
+        pipe.synchronize()
+        t0 = time.perf_counter()
+        for i in range(iters):
+            pipe.submit(h_in, h_out[i % 2])
+        pipe.synchronize()
+        dt = time.perf_counter() - t0
+        flags = pipe.device_status()
+        if flags:
+            raise RuntimeError(f"device status flags {flags:#x} in the end-to-end loop")
+        got = int(np.frombuffer(h_out[(iters - 1) % 2]["sel_offsets"].numpy().tobytes(), dtype=np.int32)[-1])
+        if got != retained:
+            raise RuntimeError(f"end-to-end loop retained {got} pairs, the device-timed step {retained}")
+    finally:
+        pipe.close()
     pairs, slowest = job_totals(retained * iters, dt, device=f"cuda:{local}")
     return {"value": pairs / slowest, "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": iters, "ms_per_step": slowest * 1e3 / iters,
-            "api": "backward_token_expert_gb300.pipeline.Recalibration.run (C ABI), pinned host buffers"}
+            "api": "backward_token_expert_gb300.pipeline.HostPipeline.submit (C ABI), pinned host buffers, "
+                   "copies on their own streams overlapping the neighbouring steps' compute"}
 
 
 # ---------------------------------------------------------------------------

@@ -1,0 +1,65 @@
+"""HostPipeline (host buffers in, host buffers out, copies overlapping the
+neighbouring batches' compute) gives, for every batch of a sequence, exactly
+the results of the single-stream path on the same inputs."""
+
+import numpy as np
+import pytest
+import torch
+
+from gpu_common import built_library, need_gpu
+from workloads import generate, get_workload
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _setup():
+    need_gpu()
+    built_library()
+
+
+def _host(inp):
+    def t(a, dtype=None):
+        x = torch.from_numpy(np.ascontiguousarray(a))
+        return (x.view(dtype) if dtype is not None else x).pin_memory()
+
+    return dict(logits=t(inp.logits), expert_idx=t(inp.expert_idx), alpha=t(inp.alpha),
+                g=t(inp.g.view(np.int16), torch.bfloat16), phi=t(inp.phi.view(np.int16), torch.bfloat16),
+                W=t(inp.W.view(np.int16), torch.bfloat16))
+
+
+@pytest.mark.parametrize("name", ["tiny_T256_E8_k2_h64_I32", "qwen3_30b_a3b_T32768_E128_k8_h2048_I768"])
+def test_every_batch_matches_the_single_stream_path(name):
+    from backward_token_expert_gb300.pipeline import OUTPUT_NAMES, HostPipeline, Recalibration, to_device_inputs
+
+    batches = [generate(get_workload(name, seed=s)) for s in (0, 1, 2)] if name.startswith("tiny") else \
+        [generate(get_workload(name, seed=s)) for s in (0, 1)]
+    w = batches[0].workload
+    order = [0, 1, 2, 1, 0] if len(batches) == 3 else [0, 1, 0]
+    pipe = HostPipeline(w.T, w.E, w.k, w.h, w.I, w.cf, w.rho)
+    hin = [_host(b) for b in batches]
+    outs = [pipe.host_outputs() for _ in order]
+    try:
+        for i, bi in enumerate(order):
+            pipe.submit(hin[bi], outs[i])
+        pipe.synchronize()
+        assert pipe.device_status() == 0
+    finally:
+        pipe.close()
+    rec = Recalibration(w.T, w.E, w.k, w.h, w.I, w.cf, w.rho)
+    try:
+        for bi, b in enumerate(batches):
+            d = to_device_inputs(b)
+            rec.run(d["logits"], d["expert_idx"], d["g"], d["phi"], d["alpha"], d["W"])
+            torch.cuda.synchronize()
+            rows = int(rec.buf.sel_offsets[-1].item())
+            for i in (i for i, x in enumerate(order) if x == bi):
+                o = outs[i]
+                assert torch.equal(o["sel_offsets"], rec.buf.sel_offsets.cpu())
+                assert torch.equal(o["sel_ids"][:rows], rec.buf.sel_ids[:rows].cpu())
+                assert torch.equal(o["summary"], rec.buf.summary.cpu())
+                assert torch.equal(o["dphi_c"][:rows].view(torch.int16), rec.buf.dphi_c[:rows].cpu().view(torch.int16))
+                assert torch.equal(o["dW"], rec.buf.dW.cpu())
+        assert set(OUTPUT_NAMES) == set(outs[0])
+    finally:
+        rec.close()
