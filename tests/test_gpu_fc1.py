@@ -116,3 +116,43 @@ def test_fc1_qwen3_layer_sampled_experts():
     nz = np.flatnonzero(q > 0)
     experts = sorted({int(nz[np.argmax(q[nz])]), int(nz[np.argmin(q[nz])]), int(nz[len(nz) // 2])})
     _fc1_check(inp, fc1_inputs(w), experts)
+
+
+def test_fc1_deepseek_v2_layer_sampled_experts():
+    # 2I = 3072 and h = 5120: the FC1 GEMMs with K = 3072 and 20 output tiles of h
+    inp = generate("deepseek_v2_T32768_E160_k6_h5120_I1536")
+    w = inp.workload
+    st = O.route_stats(inp.logits, inp.expert_idx, w.E, w.cf, w.rho)
+    q = np.asarray(st["quota"])
+    nz = np.flatnonzero(q > 0)
+    experts = sorted({int(nz[np.argmax(q[nz])]), int(nz[np.argmin(q[nz])])})
+    _fc1_check(inp, fc1_inputs(w), experts)
+
+
+def test_fc1_single_expert_top1():
+    inp = custom_inputs(T=700, E=1, k=1, h=64, I=40, rho=Fraction(2, 3), seed=53)
+    _fc1_check(inp, fc1_inputs(inp.workload))
+
+
+def test_fc1_nothing_retained_gives_exact_zeros():
+    from backward_token_expert_gb300.pipeline import Recalibration, to_device_inputs
+
+    inp = custom_inputs(T=400, E=6, k=2, h=64, I=48, seed=54)
+    w = inp.workload
+    f1 = fc1_inputs(w)
+    rec = Recalibration(w.T, w.E, w.k, w.h, w.I, w.cf, w.rho)
+    try:
+        d = to_device_inputs(inp)
+        rec.route_stats(d["logits"], d["expert_idx"], quota_override=torch.zeros(w.E, dtype=torch.int32, device="cuda"))
+        rec.backward_steps(d["g"], d["phi"], d["alpha"], d["W"])
+        f = rec._fc1_buffers()
+        f.dx.fill_(1.0)  # must come back as zeros
+        f.dW1.fill_(1.0)
+        rec.fc1_backward(_dev(f1.x), _dev(f1.ab), _dev(f1.W1))
+        torch.cuda.synchronize()
+        assert rec.device_status() == 0
+        assert int(rec.buf.sel_offsets[-1].item()) == 0
+        assert torch.count_nonzero(rec.fc1.dW1).item() == 0
+        assert torch.count_nonzero(rec.fc1.dx).item() == 0
+    finally:
+        rec.close()
