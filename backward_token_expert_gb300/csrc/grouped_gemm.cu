@@ -116,11 +116,45 @@ __device__ __forceinline__ void segment(const int32_t* __restrict__ sel_offsets,
   len = en - st;
 }
 
-template <int BN>
+// dW element type: fp32, or bf16 (round to nearest even) when OutT is uint16_t
+template <typename OutT>
+struct DwStore;
+template <>
+struct DwStore<float> {
+  __device__ static __forceinline__ void put(float* o, float4 v, int accumulate) {
+    if (accumulate) {
+      const float4 old = *reinterpret_cast<const float4*>(o);
+      v.x += old.x;
+      v.y += old.y;
+      v.z += old.z;
+      v.w += old.w;
+    }
+    *reinterpret_cast<float4*>(o) = v;
+  }
+};
+template <>
+struct DwStore<uint16_t> {
+  __device__ static __forceinline__ uint32_t pack(float lo, float hi) {
+    const __nv_bfloat162 r = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&r);
+  }
+  __device__ static __forceinline__ void put(uint16_t* o, float4 v, int accumulate) {
+    if (accumulate) {
+      const uint2 old = *reinterpret_cast<const uint2*>(o);
+      v.x += __uint_as_float(old.x << 16);
+      v.y += __uint_as_float(old.x & 0xFFFF0000u);
+      v.z += __uint_as_float(old.y << 16);
+      v.w += __uint_as_float(old.y & 0xFFFF0000u);
+    }
+    *reinterpret_cast<uint2*>(o) = make_uint2(pack(v.x, v.y), pack(v.z, v.w));
+  }
+};
+
+template <int BN, typename OutT>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CfgPair<BN>::THREADS, 1)
     wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const int32_t* __restrict__ sel_offsets, int E,
-                      int h, int I, int max_rows, int accumulate, float* __restrict__ out, unsigned int* status,
+                      int h, int I, int max_rows, int accumulate, OutT* __restrict__ out, unsigned int* status,
                       unsigned long long budget_ns) {
   using C = CfgPair<BN>;
   extern __shared__ uint8_t dsmem_raw[];
@@ -401,7 +435,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CfgPair<BN>::THREADS
       int e, mt, nt;
       decode(tile, e, mt, nt);
       const int row_w = mt * 256 + static_cast<int>(rank) * 128 + q * 32;  // first dW row of this warp
-      float* obase = out + (static_cast<size_t>(e) * h + row_w) * I;
+      OutT* obase = out + (static_cast<size_t>(e) * h + row_w) * I;
       int start, len;
       segment(sel_offsets, e, max_rows, start, len);
       if (len == 0) {
@@ -413,8 +447,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CfgPair<BN>::THREADS
             for (int v = 0; v < 4; ++v) {
               const int rr = 8 * v + sub_row;
               if (row_w + rr < h)
-                *reinterpret_cast<float4*>(obase + static_cast<size_t>(rr) * I + col) =
-                    make_float4(0.f, 0.f, 0.f, 0.f);
+                DwStore<OutT>::put(obase + static_cast<size_t>(rr) * I + col, make_float4(0.f, 0.f, 0.f, 0.f), 0);
             }
           }
         }
@@ -449,15 +482,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CfgPair<BN>::THREADS
                 float4 val = make_float4(__uint_as_float(r[16 * beta + 4 * rho]), __uint_as_float(r[16 * beta + 4 * rho + 1]),
                                          __uint_as_float(r[16 * beta + 4 * rho + 2]),
                                          __uint_as_float(r[16 * beta + 4 * rho + 3]));
-                float* o = obase + static_cast<size_t>(rr) * I + col + 16 * beta;
-                if (accumulate) {
-                  const float4 old = *reinterpret_cast<const float4*>(o);
-                  val.x += old.x;
-                  val.y += old.y;
-                  val.z += old.z;
-                  val.w += old.w;
-                }
-                *reinterpret_cast<float4*>(o) = val;
+                DwStore<OutT>::put(obase + static_cast<size_t>(rr) * I + col + 16 * beta, val, accumulate);
               }
             }
           }
@@ -836,12 +861,12 @@ lrm_status encode_w(lrm_ctx* ctx, CUtensorMap* map, const void* base, uint64_t I
   return r == CUDA_SUCCESS ? LRM_OK : LRM_ERR_CUDA;
 }
 
-template <int BN>
+template <int BN, typename OutT>
 lrm_status launch_wgrad_pair(lrm_ctx* ctx, const CUtensorMap& a, const CUtensorMap& b,
-                             const int32_t* sel_offsets, const lrm_dims& d, int max_rows, int accumulate, float* out,
+                             const int32_t* sel_offsets, const lrm_dims& d, int max_rows, int accumulate, OutT* out,
                              cudaStream_t s) {
   using C = CfgPair<BN>;
-  auto kern = wgrad_pair_kernel<BN>;
+  auto kern = wgrad_pair_kernel<BN, OutT>;
   static thread_local int configured_device = -1;
   static thread_local int clusters = 0;
   if (configured_device != ctx->device) {
@@ -935,9 +960,11 @@ extern "C" lrm_status lrm_grouped_dgrad_scatter(lrm_ctx* ctx, const uint16_t* de
   return grouped_dgrad(ctx, delta_c, W, sel_offsets, dims, max_rows, dphi_rows, sel_ids, dims.T * dims.k, stream);
 }
 
-extern "C" lrm_status lrm_grouped_wgrad(lrm_ctx* ctx, const uint16_t* delta_c, const uint16_t* phi_c,
-                                        const int32_t* sel_offsets, lrm_dims dims, int32_t max_rows,
-                                        int32_t accumulate, float* dW, void* stream) {
+namespace {
+
+template <typename OutT>
+lrm_status grouped_wgrad(lrm_ctx* ctx, const uint16_t* delta_c, const uint16_t* phi_c, const int32_t* sel_offsets,
+                         lrm_dims dims, int32_t max_rows, int32_t accumulate, OutT* dW, void* stream) {
   if (ctx == nullptr) return LRM_ERR_INVALID_ARG;
   lrm_status st = check_dims(dims);
   if (st != LRM_OK) return st;
@@ -956,5 +983,19 @@ extern "C" lrm_status lrm_grouped_wgrad(lrm_ctx* ctx, const uint16_t* delta_c, c
   if ((st = encode_2d(ctx, &ma, a_base, dims.h, rows, CfgPair<256>::BKS)) != LRM_OK) return st;
   if ((st = encode_2d(ctx, &mb, b_base, dims.I, rows, CfgPair<256>::BKS)) != LRM_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return launch_wgrad_pair<256>(ctx, ma, mb, sel_offsets, dims, max_rows, accumulate, dW, s);
+  return launch_wgrad_pair<256, OutT>(ctx, ma, mb, sel_offsets, dims, max_rows, accumulate, dW, s);
+}
+
+}  // namespace
+
+extern "C" lrm_status lrm_grouped_wgrad(lrm_ctx* ctx, const uint16_t* delta_c, const uint16_t* phi_c,
+                                        const int32_t* sel_offsets, lrm_dims dims, int32_t max_rows,
+                                        int32_t accumulate, float* dW, void* stream) {
+  return grouped_wgrad<float>(ctx, delta_c, phi_c, sel_offsets, dims, max_rows, accumulate, dW, stream);
+}
+
+extern "C" lrm_status lrm_grouped_wgrad_bf16(lrm_ctx* ctx, const uint16_t* delta_c, const uint16_t* phi_c,
+                                             const int32_t* sel_offsets, lrm_dims dims, int32_t max_rows,
+                                             int32_t accumulate, uint16_t* dW, void* stream) {
+  return grouped_wgrad<uint16_t>(ctx, delta_c, phi_c, sel_offsets, dims, max_rows, accumulate, dW, stream);
 }

@@ -50,6 +50,7 @@ EXPORTED = (
     "lrm_compact",
     "lrm_grouped_dgrad",
     "lrm_grouped_wgrad",
+    "lrm_grouped_wgrad_bf16",
     "lrm_compact_padded",
     "lrm_get_device_status",
     "lrm_set_wait_budget",
@@ -129,6 +130,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "lrm_compact": ([P, P, P, P, P, P, Dims, i32, P, P, P, P], st),
         "lrm_grouped_dgrad": ([P, P, P, P, Dims, i32, P, P], st),
         "lrm_grouped_wgrad": ([P, P, P, P, Dims, i32, i32, P, P], st),
+        "lrm_grouped_wgrad_bf16": ([P, P, P, P, Dims, i32, i32, P, P], st),
         "lrm_compact_padded": ([P, P, P, P, Dims, i32, P, P, P, P], st),
         "lrm_get_device_status": ([P, P, ctypes.POINTER(ctypes.c_uint32)], st),
         "lrm_set_wait_budget": ([P, ctypes.c_uint64], st),
@@ -294,6 +296,13 @@ def lrm_grouped_wgrad(ctx, delta_c, phi_c, sel_offsets, dims: Dims, max_rows: in
     _check(load_library().lrm_grouped_wgrad(ctx, _ptr(delta_c), _ptr(phi_c), _ptr(sel_offsets), dims,
                                             int(max_rows), int(accumulate), _ptr(dW), _stream(stream)),
            "lrm_grouped_wgrad")
+
+
+def lrm_grouped_wgrad_bf16(ctx, delta_c, phi_c, sel_offsets, dims: Dims, max_rows: int, accumulate: int, dW,
+                           stream=None) -> None:
+    _check(load_library().lrm_grouped_wgrad_bf16(ctx, _ptr(delta_c), _ptr(phi_c), _ptr(sel_offsets), dims,
+                                                 int(max_rows), int(accumulate), _ptr(dW), _stream(stream)),
+           "lrm_grouped_wgrad_bf16")
 
 
 def lrm_compact_padded(ctx, delta_c, phi_c, sel_offsets, dims: Dims, C: int, delta_pad, phi_pad, pad_offsets,

@@ -213,6 +213,15 @@ class Recalibration:
         L.lrm_grouped_wgrad(self.ctx, b.delta_c, b.phi_c, b.sel_offsets, self.dims, self.max_rows, accumulate,
                             b.dW, stream)
 
+    def wgrad_bf16(self, stream=None, accumulate=0):
+        """Step 5b with the weight gradient stored as bf16 in ``self.dW_bf16``
+        ([E, h, I], allocated on first use)."""
+        b = self.buf
+        if getattr(self, "dW_bf16", None) is None:
+            self.dW_bf16 = torch.zeros(self.E, self.h, self.I, dtype=torch.bfloat16, device=b.dW.device)
+        L.lrm_grouped_wgrad_bf16(self.ctx, b.delta_c, b.phi_c, b.sel_offsets, self.dims, self.max_rows, accumulate,
+                                 self.dW_bf16, stream)
+
     def backward_steps(self, g, phi, alpha, W, stream=None, metric: int = L.METRIC_LRM, seed: int = 0):
         """score -> select -> compact -> dgrad -> wgrad (quotas already set)."""
         self.score(g, phi, alpha, stream, metric=metric, seed=seed)

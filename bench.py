@@ -341,6 +341,7 @@ def run_ours(args, rank, world, local):
         if not args.no_comparator:
             result["comparator"] = comparator(rec, d, w, retained, pk)
             result["inverse_mapping"] = inverse_mapping(rec, d, w, retained, pk)
+            result["bf16_dW"] = bf16_dw_step(rec, d, w, retained, pk, work, min(K, 100))
             result["fc1_backward"] = fc1_backward(rec, w, retained, pk)
         if not args.no_cpu_baseline:
             result["cpu_baseline"] = cpu_baseline(inp, tokens=args.ref_tokens or 8192)
@@ -356,6 +357,45 @@ def run_ours(args, rank, world, local):
         dist.barrier()
         dist.destroy_process_group()
     return result
+
+
+def bf16_dw_step(rec, d, w, retained, pk, work, iters):
+    """The same step with the weight gradient stored as bf16
+    (lrm_grouped_wgrad_bf16; the BF16 gradient of the pages' mixed-precision
+    training): the whole step timed again, and the wgrad alone with its
+    roofline (its bytes drop from 4 to 2 per dW element)."""
+    import torch
+
+    s = torch.cuda.current_stream()
+
+    def step():
+        rec.route_stats(d["logits"], d["expert_idx"])
+        rec.score(d["g"], d["phi"], d["alpha"])
+        rec.select()
+        rec.compact(d["g"], d["phi"], d["alpha"])
+        rec.dgrad(d["W"])
+        rec.wgrad_bf16()
+
+    out = {}
+    for name, fn in (("step", step), ("wgrad", rec.wgrad_bf16)):
+        for _ in range(3):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(iters):
+            fn()
+        e1.record(s)
+        e1.synchronize()
+        out[name + "_ms"] = e0.elapsed_time(e1) / iters
+    flags = rec.device_status()
+    if flags:
+        raise RuntimeError(f"device status flags {flags:#x} in the bf16-dW step")
+    nbytes = work["wgrad"][0] - 2 * w.E * w.h * w.I
+    ent = roofline_entry(nbytes, work["wgrad"][1], out["wgrad_ms"], pk, sustained=True)
+    return {"what": "route stats .. dgrad as in the timed step, then wgrad with dW stored as bf16",
+            "value": round(retained / (out["step_ms"] * 1e-3), 1), "unit": UNIT,
+            "ms_per_step": round(out["step_ms"], 5), "steps": iters,
+            "wgrad": dict(ms=round(out["wgrad_ms"], 5), **ent)}
 
 
 def inverse_mapping(rec, d, w, retained, pk, iters=20):

@@ -4,8 +4,9 @@
  *
  * Source: "LRMoE: Demand-Side Load Re-Calibration for Efficient MoE Training
  * on Memory-Constrained Nodes" (Hu et al.), sec. 3.1-3.4, Alg. 1, Fig. 4,
- * appendix 7.1-7.2; routing statistics from "Expert Parallel Math Deep" (sections on routing as an expectation over a batch, the
- * load-balancing auxiliary loss, and capacity / drop rate).
+ * appendix 7.1-7.2; routing statistics from "Expert Parallel Math Deep"
+ * (sections on routing as an expectation over a batch, the load-balancing
+ * auxiliary loss, and capacity / drop rate).
  *
  * The path, in call order on one stream, with no host synchronisation:
  *   lrm_route_stats -> lrm_score -> lrm_select -> lrm_compact
@@ -292,6 +293,20 @@ LRM_API lrm_status lrm_combine_rows(lrm_ctx* ctx, const uint16_t* rows, const in
 LRM_API lrm_status lrm_grouped_wgrad(lrm_ctx* ctx, const uint16_t* delta_c, const uint16_t* phi_c,
                              const int32_t* sel_offsets, lrm_dims dims, int32_t max_rows, int32_t accumulate,
                              float* dW, void* stream);
+
+/*
+ * Step 5b with a bf16 weight gradient: the same products accumulated in fp32
+ * in TMEM, each dW element rounded once to bf16 (nearest even) when it is
+ * stored.  The pages train in BF16 (LRMoE sec. 4.1), and TopoEP sec. 3.2
+ * counts the gradient of BF16 mixed-precision training as BF16 next to an
+ * FP32 master copy, so this is the dtype such a step hands to the optimizer;
+ * it halves the dW bytes that bound lrm_grouped_wgrad.  dW [E, h, I] bf16 bits,
+ * 16-byte aligned.  accumulate = 1 adds the fp32 products to the stored bf16
+ * values and rounds the sum.  Errors as for lrm_grouped_wgrad.
+ */
+LRM_API lrm_status lrm_grouped_wgrad_bf16(lrm_ctx* ctx, const uint16_t* delta_c, const uint16_t* phi_c,
+                                  const int32_t* sel_offsets, lrm_dims dims, int32_t max_rows, int32_t accumulate,
+                                  uint16_t* dW, void* stream);
 
 /*
  * Comparator (measurement only) - the zero-masked fixed-shape layout of
