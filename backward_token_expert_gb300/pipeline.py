@@ -244,6 +244,34 @@ class Recalibration:
         return L.lrm_get_device_status(self.ctx, stream)
 
 
+class StepGraph:
+    """The whole step (route stats through the weight gradient) captured once
+    as a CUDA graph over fixed device buffers: one launch per step instead of
+    nine library calls, so the host issues nothing per kernel.  The graph
+    reads the tensors it was captured with; a caller feeds a new batch by
+    writing into them (``copy_``) before ``replay``.  The first, eager run
+    does each kernel's one-time set-up (function attributes, occupancy), which
+    must not happen inside a capture."""
+
+    def __init__(self, rec: "Recalibration", logits, expert_idx, g, phi, alpha, W):
+        self.rec = rec
+        self.inputs = dict(logits=logits, expert_idx=expert_idx, g=g, phi=phi, alpha=alpha, W=W)
+        dev = rec.device
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            rec.run(logits, expert_idx, g, phi, alpha, W, stream=side)
+            side.synchronize()
+            with torch.cuda.graph(self.graph, stream=side):
+                rec.run(logits, expert_idx, g, phi, alpha, W, stream=side)
+        torch.cuda.current_stream(dev).wait_stream(side)
+
+    def replay(self) -> None:
+        """Enqueue one step on the current stream."""
+        self.graph.replay()
+
+
 def to_device_inputs(inp, device="cuda"):
     """Copy a workloads.Inputs record to device tensors (bf16 bits viewed as bf16)."""
     import numpy as np

@@ -63,3 +63,31 @@ def test_every_batch_matches_the_single_stream_path(name):
         assert set(OUTPUT_NAMES) == set(outs[0])
     finally:
         rec.close()
+
+
+def test_step_graph_replays_the_eager_step():
+    from backward_token_expert_gb300.pipeline import Recalibration, StepGraph, to_device_inputs
+
+    a, b = (generate(get_workload("tiny_T256_E8_k2_h64_I32", seed=s)) for s in (3, 4))
+    w = a.workload
+    rec = Recalibration(w.T, w.E, w.k, w.h, w.I, w.cf, w.rho)
+    eager = Recalibration(w.T, w.E, w.k, w.h, w.I, w.cf, w.rho)
+    try:
+        d = to_device_inputs(a)
+        graph = StepGraph(rec, d["logits"], d["expert_idx"], d["g"], d["phi"], d["alpha"], d["W"])
+        for inp in (b, a, b):  # new batches written into the captured buffers
+            src = to_device_inputs(inp)
+            for name, t in graph.inputs.items():
+                t.copy_(src[name])
+            graph.replay()
+            eager.run(src["logits"], src["expert_idx"], src["g"], src["phi"], src["alpha"], src["W"])
+            torch.cuda.synchronize()
+            assert torch.equal(rec.buf.sel_offsets, eager.buf.sel_offsets)
+            rows = int(eager.buf.sel_offsets[-1].item())
+            assert torch.equal(rec.buf.sel_ids[:rows], eager.buf.sel_ids[:rows])
+            assert torch.equal(rec.buf.dW, eager.buf.dW)
+            assert torch.equal(rec.buf.dphi_c[:rows].view(torch.int16), eager.buf.dphi_c[:rows].view(torch.int16))
+        assert rec.device_status() == 0 and eager.device_status() == 0
+    finally:
+        rec.close()
+        eager.close()
