@@ -82,6 +82,103 @@ __global__ void __launch_bounds__(CP_THREADS) compact_kernel(
   }
 }
 
+// TMA-staged gather (the default when a row pair fits the ring): each warp
+// owns a ring of `depth` slots in shared memory, one retained row per slot.
+// Lane 0 fetches the row's g_t and phi_u with two bulk copies that complete
+// on the slot's mbarrier; the warp scales g_t by alpha_u in place (fp32
+// multiply, round to nearest even); lane 0 then writes the slot out to
+// delta_c[r] and phi_c[r] with two bulk stores and, once the previous row's
+// stores have read their slot, refills that slot with the row `depth` ahead.
+// The copies run in the async proxy, so each warp keeps up to `depth` rows
+// of loads and stores in flight with one thread issuing them.
+constexpr int CT_WARPS = 4;
+constexpr int CT_THREADS = 32 * CT_WARPS;
+constexpr int CT_MAX_DEPTH = 4;
+
+__global__ void __launch_bounds__(CT_THREADS) compact_tma_kernel(
+    const uint8_t* __restrict__ g, const uint8_t* __restrict__ phi, const float* __restrict__ alpha,
+    const int32_t* __restrict__ sel_offsets, const int32_t* __restrict__ sel_ids, int E, int N, int k,
+    uint32_t gbytes, uint32_t pbytes, uint32_t slot_bytes, int depth, int max_rows, uint8_t* __restrict__ delta_c,
+    uint8_t* __restrict__ phi_c, float* __restrict__ alpha_c, unsigned int* status, unsigned long long budget_ns) {
+  extern __shared__ __align__(128) uint8_t ct_smem[];
+  __shared__ __align__(8) uint64_t bars[CT_WARPS][CT_MAX_DEPTH];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int total = __ldg(sel_offsets + E);
+  if (total > max_rows) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) raise_flag(status, LRM_ERR_SHAPE);
+    total = max_rows;
+  }
+  if (lane == 0) {
+    for (int s = 0; s < depth; ++s) mbar_init(&bars[warp][s], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  uint8_t* ring = ct_smem + static_cast<size_t>(warp) * depth * slot_bytes;
+  const uint32_t g_off = (gbytes + 127u) & ~127u;  // phi part of a slot
+  const int gw = blockIdx.x * CT_WARPS + warp;
+  const int W = gridDim.x * CT_WARPS;
+  const int n_rows = gw < total ? (total - gw + W - 1) / W : 0;  // rows gw, gw + W, ...
+
+  // lane 0: fetch the i-th row of this warp into slot i % depth
+  auto issue = [&](int i) {
+    uint64_t* bar = &bars[warp][i % depth];
+    uint8_t* slot = ring + static_cast<size_t>(i % depth) * slot_bytes;
+    const int u = __ldg(sel_ids + gw + static_cast<size_t>(i) * W);
+    if (u < 0 || u >= N) {
+      raise_flag(status, LRM_ERR_INDEX);
+      mbar_arrive(bar);  // completes the phase with nothing loaded; the row is skipped
+      return;
+    }
+    mbar_arrive_expect_tx(bar, gbytes + pbytes);
+    bulk_load(slot, g + static_cast<size_t>(u / k) * gbytes, gbytes, bar);
+    bulk_load(slot + g_off, phi + static_cast<size_t>(u) * pbytes, pbytes, bar);
+  };
+  if (lane == 0)
+    for (int i = 0; i < depth && i < n_rows; ++i) issue(i);
+  int issued = depth < n_rows ? depth : n_rows;
+
+  int i = 0;
+  for (; i < n_rows; ++i) {
+    const int s = i % depth;
+    const bool got = mbar_wait(&bars[warp][s], static_cast<uint32_t>(i / depth) & 1u, budget_ns, nullptr);
+    if (!__all_sync(0xffffffffu, got)) {  // the whole warp leaves together
+      if (lane == 0) raise_flag(status, LRM_ERR_TIMEOUT);
+      break;
+    }
+    const size_t r = gw + static_cast<size_t>(i) * W;
+    const int u = __ldg(sel_ids + r);
+    uint8_t* slot = ring + static_cast<size_t>(s) * slot_bytes;
+    if (u >= 0 && u < N) {
+      const float a = __ldg(alpha + u);
+      uint4* gv = reinterpret_cast<uint4*>(slot);
+      for (uint32_t v = lane; v < gbytes / 16; v += 32) gv[v] = scale_bf16x8(gv[v], a);
+      fence_proxy_async_smem();  // the scaled row, written by the warp, is read by the bulk store
+      __syncwarp();
+      if (lane == 0) {
+        bulk_store(delta_c + r * gbytes, slot, gbytes);
+        bulk_store(phi_c + r * pbytes, slot + g_off, pbytes);
+        if (alpha_c != nullptr) alpha_c[r] = a;
+      }
+    }
+    if (lane == 0) {
+      bulk_commit();  // one group per row (empty for a skipped row)
+      // the previous row's stores have read their slot: refill it `depth` rows ahead
+      if (i >= 1 && issued < n_rows) {
+        bulk_wait_read<1>();
+        issue(issued);
+        ++issued;
+      }
+    }
+    __syncwarp();
+  }
+  if (lane == 0) {
+    // after a timeout, let the fetches already issued land before the block exits
+    for (int j = i; j < issued; ++j)
+      if (!mbar_wait(&bars[warp][j % depth], static_cast<uint32_t>(j / depth) & 1u, budget_ns, nullptr)) break;
+    bulk_wait<0>();
+  }
+}
+
 __global__ void __launch_bounds__(CP_THREADS) compact_padded_kernel(
     const uint4* __restrict__ delta_c, const uint4* __restrict__ phi_c, const int32_t* __restrict__ sel_offsets,
     int E, int C, int hv, int iv, uint4* __restrict__ delta_pad, uint4* __restrict__ phi_pad,
@@ -136,6 +233,35 @@ extern "C" lrm_status lrm_compact(lrm_ctx* ctx, const uint16_t* g, const uint16_
     return LRM_ERR_ALIGN;
   DeviceGuard guard(ctx->device);
   if (!guard.ok) return LRM_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // TMA-staged gather when a ring of at least two row slots per warp fits in
+  // shared memory (every shape up to h + I of about 13k)
+  const uint32_t gbytes = static_cast<uint32_t>(dims.h) * 2, pbytes = static_cast<uint32_t>(dims.I) * 2;
+  const uint32_t slot = ((gbytes + 127u) & ~127u) + ((pbytes + 127u) & ~127u);
+  const size_t smem_cap = static_cast<size_t>(ctx->smem_optin) - 1024;  // static barriers and slack
+  int depth = CT_MAX_DEPTH;
+  while (depth >= 2 && static_cast<size_t>(CT_WARPS) * depth * slot > smem_cap) --depth;
+  if (depth >= 2) {
+    static thread_local int tma_device = -1;
+    if (tma_device != ctx->device) {
+      LRM_CHECK_CUDA(cudaFuncSetAttribute(compact_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          static_cast<int>(smem_cap)));
+      tma_device = ctx->device;
+    }
+    const size_t smem = static_cast<size_t>(CT_WARPS) * depth * slot;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, compact_tma_kernel, CT_THREADS, smem) != cudaSuccess ||
+        per_sm < 1)
+      per_sm = 1;
+    const long long need = (static_cast<long long>(max_rows) + CT_WARPS - 1) / CT_WARPS;
+    const long long cap = static_cast<long long>(per_sm) * ctx->sm_count;
+    const int grid = static_cast<int>(need < cap ? need : cap);
+    compact_tma_kernel<<<grid, CT_THREADS, smem, s>>>(
+        reinterpret_cast<const uint8_t*>(g), reinterpret_cast<const uint8_t*>(phi), alpha, sel_offsets, sel_ids,
+        dims.E, dims.T * dims.k, dims.k, gbytes, pbytes, slot, depth, max_rows, reinterpret_cast<uint8_t*>(delta_c),
+        reinterpret_cast<uint8_t*>(phi_c), alpha_c, ctx->d_status, ctx->wait_budget_ns);
+    return launch_status();
+  }
   static thread_local int cap_device = -1, cap = 0;
   if (cap_device != ctx->device) {
     cap = resident_grid(ctx, compact_kernel, CP_THREADS, 0);
@@ -143,7 +269,7 @@ extern "C" lrm_status lrm_compact(lrm_ctx* ctx, const uint16_t* g, const uint16_
   }
   const int need = (max_rows + CP_WARPS - 1) / CP_WARPS;
   const int grid = need < cap ? need : cap;
-  compact_kernel<<<grid, CP_THREADS, 0, static_cast<cudaStream_t>(stream)>>>(
+  compact_kernel<<<grid, CP_THREADS, 0, s>>>(
       reinterpret_cast<const uint4*>(g), reinterpret_cast<const uint4*>(phi), alpha, sel_offsets, sel_ids,
       dims.E, dims.T * dims.k, dims.k, dims.h / 8, dims.I / 8, max_rows, reinterpret_cast<uint4*>(delta_c),
       reinterpret_cast<uint4*>(phi_c), alpha_c, ctx->d_status);
