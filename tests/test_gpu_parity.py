@@ -68,6 +68,12 @@ def test_wide_expert_uses_256_column_tiles():
     full_check(custom_inputs(T=4096, E=8, k=2, h=256, I=768, s=0.5, rho=Fraction(1, 2), seed=2))
 
 
+def test_rows_too_wide_for_the_staging_ring():
+    # h + I = 17408: a g row and a phi row no longer fit two slots per warp of
+    # the TMA-staged compaction, so the 128-bit copy kernel does it
+    full_check(custom_inputs(T=192, E=4, k=2, h=16384, I=1024, s=0.5, rho=Fraction(3, 4), seed=7))
+
+
 def test_non_power_of_two_experts_and_k():
     full_check(custom_inputs(T=999, E=20, k=6, h=136, I=1408, s=1.2, rho=Fraction(3, 5), seed=3,
                              phi_scale="lognormal"))
