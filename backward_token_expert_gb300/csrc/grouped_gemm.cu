@@ -566,7 +566,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CfgDgradPair<BNR>::T
   __shared__ uint32_t s_tmem_base;
   __shared__ int s_abort;
   __shared__ int s_len[MAX_E];
-  __shared__ uint16_t s_order[MAX_E];  // experts by descending retained rows (ties: lower id)
+  __shared__ uint16_t s_order[MAX_E];  // experts in schedule order (descending index)
   __shared__ int s_prefix[MAX_E + 1];  // first pair tile of the expert at each position of s_order
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -575,23 +575,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CfgDgradPair<BNR>::T
   const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
   const int tiles_m = (I + 255) / 256;  // pair tiles over the expert width
 
-  // Schedule: experts heaviest first (so the short tiles of light experts
-  // even out the end), the tiles of one expert side by side (they share W_e
-  // through L2), dealt round robin to the pairs.
+  // Schedule: experts in descending index order, the tiles of one expert
+  // side by side (they share W_e through L2), dealt round robin to the pairs.
+  // Compaction writes the segments in ascending expert order, so the ones it
+  // wrote last are still in L2 when dgrad starts (4-6 % faster than a
+  // heaviest-first order, measured); the tiles cost nearly the same whatever
+  // the expert, so the order does not unbalance the pairs.
   for (int e = tid; e < E; e += C::THREADS) {
     int st, ln;
     segment(sel_offsets, e, max_rows, st, ln);
     s_len[e] = ln;
-  }
-  __syncthreads();
-  for (int e = tid; e < E; e += C::THREADS) {
-    const int le = s_len[e];
-    int pos = 0;
-    for (int x = 0; x < E; ++x) {
-      const int lx = s_len[x];
-      pos += (lx > le) || (lx == le && x < e);
-    }
-    s_order[pos] = static_cast<uint16_t>(e);
+    s_order[E - 1 - e] = static_cast<uint16_t>(e);
   }
   __syncthreads();
   if (warp == 0) {
