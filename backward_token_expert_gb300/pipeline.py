@@ -301,16 +301,24 @@ class HostPipeline:
     Two slots (each a ``Recalibration`` with its own device inputs and
     outputs) alternate; events order every reuse: a slot's inputs are not
     overwritten before its last compute has read them, and its outputs are
-    not recomputed before they were copied out.  ``submit`` only enqueues;
-    the caller keeps each host buffer untouched until ``synchronize`` (or
-    until two later submits have completed).  Host buffers should be pinned
-    for the copies to run asynchronously.
+    not recomputed before they were copied out.  Of the compacted input
+    gradient only the retained rows go back: a batch's small outputs (the
+    selection offsets first) are copied right after its compute, and its
+    ``dphi_c`` rows are copied, exactly ``sel_offsets[E]`` of them, when the
+    next batch is submitted (or at ``synchronize``), once that count is on
+    the host.  ``submit`` otherwise only enqueues; the caller keeps each host
+    buffer untouched until ``synchronize`` (or until two later submits have
+    returned).  Host buffers should be pinned for the copies to run
+    asynchronously.
     """
+
+    SMALL = ("sel_offsets", "summary", "sel_ids")
 
     def __init__(self, T, E, k, h, I, cf=Fraction(5, 4), rho=Fraction(3, 4), device=0):
         self.recs = [Recalibration(T, E, k, h, I, cf, rho, device=device) for _ in range(2)]
         dev = self.recs[0].device
         self.device = dev
+        self.E = int(E)
         N = int(T) * int(k)
         bf = dict(dtype=torch.bfloat16, device=dev)
         self.dev_in = [dict(logits=torch.empty(T, E, dtype=torch.float32, device=dev),
@@ -319,13 +327,30 @@ class HostPipeline:
                             alpha=torch.empty(N, dtype=torch.float32, device=dev), W=torch.empty(E, h, I, **bf))
                        for _ in range(2)]
         self.s_in, self.s_comp, self.s_out = (torch.cuda.Stream(dev) for _ in range(3))
-        self.ev_in, self.ev_comp, self.ev_out = ([torch.cuda.Event() for _ in range(2)] for _ in range(3))
+        self.ev_in, self.ev_comp, self.ev_out, self.ev_small = (
+            [torch.cuda.Event() for _ in range(2)] for _ in range(4))
         self.submitted = 0
+        self.pending = None  # (slot, host_out) whose dphi_c rows are still to be copied
+        self.d2h_bytes = 0  # device -> host bytes enqueued so far
+
+    def _flush(self) -> None:
+        if self.pending is None:
+            return
+        s, host_out = self.pending
+        self.pending = None
+        self.ev_small[s].synchronize()  # the batch's selection offsets are on the host
+        rows = int(host_out["sel_offsets"][self.E])
+        rows = max(0, min(rows, host_out["dphi_c"].shape[0]))
+        with torch.cuda.stream(self.s_out):
+            if rows:
+                host_out["dphi_c"][:rows].copy_(self.recs[s].buf.dphi_c[:rows], non_blocking=True)
+        self.d2h_bytes += rows * host_out["dphi_c"].stride(0) * host_out["dphi_c"].element_size()
+        self.ev_out[s].record(self.s_out)
 
     def submit(self, host_in: dict, host_out: dict) -> int:
         """Enqueue one batch: copy `host_in` (the six inputs, by name) in, run
-        the path, copy the results into `host_out` (dW, dphi_c, sel_offsets,
-        sel_ids, summary).  Returns the slot used."""
+        the path, copy the results into `host_out` (dW, the retained rows of
+        dphi_c, sel_offsets, sel_ids, summary).  Returns the slot used."""
         s = self.submitted % 2
         rec, din = self.recs[s], self.dev_in[s]
         reuse = self.submitted >= 2
@@ -340,12 +365,17 @@ class HostPipeline:
             self.s_comp.wait_event(self.ev_out[s])
         rec.run(din["logits"], din["expert_idx"], din["g"], din["phi"], din["alpha"], din["W"], stream=self.s_comp)
         self.ev_comp[s].record(self.s_comp)
+        # the previous batch's retained rows go out first, then this batch's outputs
+        self._flush()
         self.s_out.wait_event(self.ev_comp[s])
         b = rec.buf
         with torch.cuda.stream(self.s_out):
-            for name in OUTPUT_NAMES:
+            for name in self.SMALL:
                 host_out[name].copy_(getattr(b, name), non_blocking=True)
-        self.ev_out[s].record(self.s_out)
+            self.ev_small[s].record(self.s_out)
+            host_out["dW"].copy_(b.dW, non_blocking=True)
+        self.d2h_bytes += sum(host_out[n].numel() * host_out[n].element_size() for n in self.SMALL + ("dW",))
+        self.pending = (s, host_out)
         self.submitted += 1
         return s
 
@@ -356,6 +386,7 @@ class HostPipeline:
         return {k2: v.pin_memory() for k2, v in out.items()} if pin else out
 
     def synchronize(self) -> None:
+        self._flush()
         for st in (self.s_in, self.s_comp, self.s_out):
             st.synchronize()
 
