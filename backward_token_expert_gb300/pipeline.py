@@ -222,18 +222,23 @@ class Recalibration:
         L.lrm_grouped_wgrad_bf16(self.ctx, b.delta_c, b.phi_c, b.sel_offsets, self.dims, self.max_rows, accumulate,
                                  self.dW_bf16, stream)
 
-    def backward_steps(self, g, phi, alpha, W, stream=None, metric: int = L.METRIC_LRM, seed: int = 0):
-        """score -> select -> compact -> dgrad -> wgrad (quotas already set)."""
+    def backward_steps(self, g, phi, alpha, W, stream=None, metric: int = L.METRIC_LRM, seed: int = 0,
+                       dw_bf16: bool = False):
+        """score -> select -> compact -> dgrad -> wgrad (quotas already set);
+        with `dw_bf16` the weight gradient goes to ``self.dW_bf16``."""
         self.score(g, phi, alpha, stream, metric=metric, seed=seed)
         self.select(stream)
         self.compact(g, phi, alpha, stream)
         self.dgrad(W, stream)
-        self.wgrad(stream)
+        if dw_bf16:
+            self.wgrad_bf16(stream)
+        else:
+            self.wgrad(stream)
 
-    def run(self, logits, expert_idx, g, phi, alpha, W, stream=None):
+    def run(self, logits, expert_idx, g, phi, alpha, W, stream=None, dw_bf16: bool = False):
         """The whole path, enqueued on one stream."""
         self.route_stats(logits, expert_idx, stream)
-        self.backward_steps(g, phi, alpha, W, stream)
+        self.backward_steps(g, phi, alpha, W, stream, dw_bf16=dw_bf16)
 
     def summary(self) -> dict:
         raw = bytes(self.buf.summary.cpu().numpy().tobytes())
@@ -253,7 +258,7 @@ class StepGraph:
     does each kernel's one-time set-up (function attributes, occupancy), which
     must not happen inside a capture."""
 
-    def __init__(self, rec: "Recalibration", logits, expert_idx, g, phi, alpha, W):
+    def __init__(self, rec: "Recalibration", logits, expert_idx, g, phi, alpha, W, dw_bf16: bool = False):
         self.rec = rec
         self.inputs = dict(logits=logits, expert_idx=expert_idx, g=g, phi=phi, alpha=alpha, W=W)
         dev = rec.device
@@ -261,10 +266,10 @@ class StepGraph:
         side.wait_stream(torch.cuda.current_stream(dev))
         self.graph = torch.cuda.CUDAGraph()
         with torch.cuda.stream(side):
-            rec.run(logits, expert_idx, g, phi, alpha, W, stream=side)
+            rec.run(logits, expert_idx, g, phi, alpha, W, stream=side, dw_bf16=dw_bf16)
             side.synchronize()
             with torch.cuda.graph(self.graph, stream=side):
-                rec.run(logits, expert_idx, g, phi, alpha, W, stream=side)
+                rec.run(logits, expert_idx, g, phi, alpha, W, stream=side, dw_bf16=dw_bf16)
         torch.cuda.current_stream(dev).wait_stream(side)
 
     def replay(self) -> None:

@@ -395,22 +395,16 @@ def run_ours(args, rank, world, local):
 def bf16_dw_step(rec, d, w, retained, pk, work, iters):
     """The same step with the weight gradient stored as bf16
     (lrm_grouped_wgrad_bf16; the BF16 gradient of the pages' mixed-precision
-    training): the whole step timed again, and the wgrad alone with its
-    roofline (its bytes drop from 4 to 2 per dW element)."""
+    training): the whole step as a CUDA graph timed again, and the wgrad alone
+    with its roofline (its bytes drop from 4 to 2 per dW element)."""
     import torch
 
+    from backward_token_expert_gb300.pipeline import StepGraph
+
     s = torch.cuda.current_stream()
-
-    def step():
-        rec.route_stats(d["logits"], d["expert_idx"])
-        rec.score(d["g"], d["phi"], d["alpha"])
-        rec.select()
-        rec.compact(d["g"], d["phi"], d["alpha"])
-        rec.dgrad(d["W"])
-        rec.wgrad_bf16()
-
+    graph = StepGraph(rec, d["logits"], d["expert_idx"], d["g"], d["phi"], d["alpha"], d["W"], dw_bf16=True)
     out = {}
-    for name, fn in (("step", step), ("wgrad", rec.wgrad_bf16)):
+    for name, fn in (("step", graph.replay), ("wgrad", rec.wgrad_bf16)):
         for _ in range(3):
             fn()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -425,7 +419,7 @@ def bf16_dw_step(rec, d, w, retained, pk, work, iters):
         raise RuntimeError(f"device status flags {flags:#x} in the bf16-dW step")
     nbytes = work["wgrad"][0] - 2 * w.E * w.h * w.I
     ent = roofline_entry(nbytes, work["wgrad"][1], out["wgrad_ms"], pk, sustained=True)
-    return {"what": "route stats .. dgrad as in the timed step, then wgrad with dW stored as bf16",
+    return {"what": "the timed step (CUDA graph) with dW stored as bf16",
             "value": round(retained / (out["step_ms"] * 1e-3), 1), "unit": UNIT,
             "ms_per_step": round(out["step_ms"], 5), "steps": iters,
             "wgrad": dict(ms=round(out["wgrad_ms"], 5), **ent)}
