@@ -117,7 +117,8 @@ __global__ void __launch_bounds__(CT_THREADS) compact_tma_kernel(
   const uint32_t g_off = (gbytes + 127u) & ~127u;  // phi part of a slot
   const int gw = blockIdx.x * CT_WARPS + warp;
   const int W = gridDim.x * CT_WARPS;
-  const int n_rows = gw < total ? (total - gw + W - 1) / W : 0;  // rows gw, gw + W, ...
+  // rows gw, gw + W, ... of this warp
+  const int n_rows = gw < total ? static_cast<int>((static_cast<long long>(total) - gw + W - 1) / W) : 0;
 
   // lane 0: fetch the i-th row of this warp into slot i % depth
   auto issue = [&](int i) {
