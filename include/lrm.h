@@ -37,6 +37,11 @@
  *    that word with lrm_get_device_status.  No call traps or hangs the GPU.
  *  - Ragged totals (sum of quotas, per-expert row counts) stay on the device;
  *    the caller passes max_rows, an upper bound used to size buffers.
+ *  - Because no call but lrm_get_device_status synchronises with the host, a
+ *    sequence of calls can be captured into a CUDA graph.  The first call of
+ *    each kind on a device also sets up its kernels (function attributes,
+ *    occupancy queries) on the host; make one call of each kind before
+ *    capturing, so that the capture holds the launches only.
  */
 #ifndef LRM_H
 #define LRM_H
