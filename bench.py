@@ -330,6 +330,7 @@ def run_ours(args, rank, world, local):
                    peak_kind="sustained bf16 (of measured)" if top["bound"] == "tensor" else "hbm copy (of measured)",
                    peak_source=pk["source"])
         value = job_pairs / job_s
+        in_bytes = w.N * w.I * 2 + w.E * w.h * w.I * 2 + w.T * w.h * 2
         # pipeline fraction: the time every step would take at its binding roof,
         # over the measured time of the steps
         ideal_s = sum(max(work[n][0] / (pk["hbm"] * 1e9), work[n][1] / (pk["bf16_sustained"] * 1e12))
@@ -348,13 +349,15 @@ def run_ours(args, rank, world, local):
             "scaling": "weak",
             "vs_baseline": None,
             "dtype": "bf16",
-            "data": "synthetic (seeded; Qwen3-30B-A3B-shaped layer, random-init weights)",
+            "data": f"synthetic (seeded {w.name} layer, random-init weights)",
             "config": {
                 "workload": w.name, "T": w.T, "E": w.E, "k": w.k, "h": w.h, "I": w.I,
                 "zipf_s": w.zipf_s, "rho": str(w.rho), "CF": str(w.cf), "retained_pairs": retained,
                 "routed_pairs": w.N, "C": summ["C"], "max_over_mean": round(summ["max_over_mean"], 3),
                 "drop_rate": round(summ["drop_rate"], 5), "parallelism": f"replicas x{world}",
-                "l2": "no flush: inputs larger than L2 (phi 384 MiB, W 384 MiB, g 128 MiB)",
+                "l2": (f"no flush: inputs {'larger than' if in_bytes > 129e6 else 'within'} L2 "
+                       f"(phi {w.N * w.I * 2 / 2**20:.0f} MiB, W {w.E * w.h * w.I * 2 / 2**20:.0f} MiB, "
+                       f"g {w.T * w.h * 2 / 2**20:.0f} MiB; L2 129 MB)"),
             },
             "roofline": top,
             "launch": "CUDA graph of the whole step (StepGraph.replay); per-kernel times from the same step "
