@@ -38,6 +38,10 @@ constexpr int SEL_MAX_BINS = 2048;
 constexpr int GATHER_THREADS = 256;
 constexpr int SEL_REGION = 192;                         // candidate keys (and positions) a warp may keep
 constexpr int SEL_CAND_KEYS = SEL_REGION * SEL_WARPS;
+// regions of an expert whose keys are not cached: they take the key cache's
+// shared memory (keys, then positions), 4.4 times the room
+constexpr int SEL_BIG_REGION = 848;
+static_assert(SEL_BIG_REGION * SEL_WARPS * 6 <= SEL_SMEM_KEYS * 4, "big regions fit the key cache");
 constexpr int SEL_LOAD = 8;                             // keys per thread in flight while loading an expert
 constexpr int SEL_OUT_UNROLL = 16;   // 32-candidate steps whose loads are issued together
 constexpr int SEL_SAMPLE_MIN = 4096; // experts with more candidates bracket the boundary by sampling
@@ -167,6 +171,12 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
   warp_range(n, warp, w0, w1);
   uint32_t* region = s_cand + warp * SEL_REGION;
   uint16_t* region_pos = s_cpos + warp * SEL_REGION;
+  int reg_cap = SEL_REGION;
+  if (n > SEL_SMEM_KEYS) {  // the keys stay in global memory: the cache's space holds the regions
+    reg_cap = SEL_BIG_REGION;
+    region = s_keys + warp * SEL_BIG_REGION;
+    region_pos = reinterpret_cast<uint16_t*>(s_keys + SEL_WARPS * SEL_BIG_REGION) + warp * SEL_BIG_REGION;
+  }
 
   uint32_t prefix = 0, mask = 0;
   int want = q;  // keys still to take among the radix candidates
@@ -175,7 +185,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
   bool bracketed = false;   // the radix candidates are the sample bracket's keys
   uint32_t cand_hi = 0xFFFFFFFFu;  // keys above this are kept without being radix candidates
   int w_cap = 0;            // this warp's captured keys (at or above the bracket's low key)
-  if (n > SEL_SAMPLE_MIN) {
+  if (n > SEL_SAMPLE_MIN && (n + SEL_WARPS - 1) / SEL_WARPS <= 65535) {  // positions fit 16 bits
     // Sample select: sort 1024 evenly spaced keys (descending, bitonic), take
     // the sample keys a few standard deviations either side of the expected
     // rank of the boundary as a bracket [lo, hi].  One pass counts the keys
@@ -221,7 +231,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
       const bool cap = live && kk >= lo;
       const unsigned bc = __ballot_sync(0xffffffffu, cap);
       const int pos = w_cap + __popc(bc & lt_mask);
-      if (cap && pos < SEL_REGION) {
+      if (cap && pos < reg_cap) {
         region[pos] = kk;
         region_pos[pos] = static_cast<uint16_t>(i - w0);
       }
@@ -236,7 +246,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
     warp_totals_prefix(s_wgt, warp, lane, &c_gt);
     warp_totals_prefix(s_weq, warp, lane, &c_cap);
     const int max_cap = __reduce_max_sync(0xffffffffu, s_weq[lane]);
-    if (c_gt < q && q <= c_cap && max_cap <= SEL_REGION) {
+    if (c_gt < q && q <= c_cap && max_cap <= reg_cap) {
       bracketed = true;
       want = q - c_gt;
       ge_floor = lo;
@@ -298,7 +308,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
       }
       if (lo_bit == 0) break;
       // once the boundary bin is small, each warp keeps only its keys of it
-      if (!in_regions && bincnt <= SEL_CAND_KEYS) {
+      if (!in_regions && bincnt <= reg_cap * SEL_WARPS) {
         int c = 0;
 #pragma unroll 4
         for (int i = lane; i - lane < ncand; i += 32) {
@@ -306,10 +316,10 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
           const bool m = i < ncand && (kk & mask) == prefix;
           const unsigned bm = __ballot_sync(0xffffffffu, m);
           const int pos = c + __popc(bm & lt_mask);
-          if (m && pos < SEL_REGION) region[pos] = kk;
+          if (m && pos < reg_cap) region[pos] = kk;
           c += __popc(bm);
         }
-        if (!__syncthreads_or(c > SEL_REGION)) {
+        if (!__syncthreads_or(c > reg_cap)) {
           cand = region;
           ncand = c;
           in_regions = true;
