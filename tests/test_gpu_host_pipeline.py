@@ -65,10 +65,12 @@ def test_every_batch_matches_the_single_stream_path(name):
         rec.close()
 
 
-def test_step_graph_replays_the_eager_step():
+@pytest.mark.parametrize("name", ["tiny_T256_E8_k2_h64_I32", "qwen3_30b_a3b_T32768_E128_k8_h2048_I768"])
+def test_step_graph_replays_the_eager_step(name):
+    # the graph is the launch configuration the bench times
     from backward_token_expert_gb300.pipeline import Recalibration, StepGraph, to_device_inputs
 
-    a, b = (generate(get_workload("tiny_T256_E8_k2_h64_I32", seed=s)) for s in (3, 4))
+    a, b = (generate(get_workload(name, seed=s)) for s in (3, 4))
     w = a.workload
     rec = Recalibration(w.T, w.E, w.k, w.h, w.I, w.cf, w.rho)
     eager = Recalibration(w.T, w.E, w.k, w.h, w.I, w.cf, w.rho)
