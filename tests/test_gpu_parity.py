@@ -14,7 +14,6 @@ import pytest
 import oracle as O
 from gpu_common import (
     SCORE_RTOL,
-    bf16_np,
     built_library,
     check_compaction,
     check_gemms,
@@ -156,7 +155,6 @@ def test_zero_masked_comparator_matches_compacted():
 def test_wgrad_accumulate_adds_into_dW():
     import torch
 
-    from backward_token_expert_gb300 import lrm as L
     from backward_token_expert_gb300.pipeline import Recalibration, to_device_inputs
 
     inp = custom_inputs(T=512, E=4, k=2, h=128, I=128, seed=10)
