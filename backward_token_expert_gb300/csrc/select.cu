@@ -43,7 +43,8 @@ constexpr int SEL_CAND_KEYS = SEL_REGION * SEL_WARPS;
 constexpr int SEL_BIG_REGION = 848;
 static_assert(SEL_BIG_REGION * SEL_WARPS * 6 <= SEL_SMEM_KEYS * 4, "big regions fit the key cache");
 constexpr int SEL_LOAD = 8;                             // keys per thread in flight while loading an expert
-constexpr int SEL_OUT_UNROLL = 16;   // 32-candidate steps whose loads are issued together
+constexpr int SEL_OUT_UNROLL = 4;    // 32-candidate steps whose loads are issued together (more than 4
+                                     // leaves too few of the 64 registers for the loads to overlap)
 constexpr int SEL_SAMPLE_MIN = 4096; // experts with more candidates bracket the boundary by sampling
 
 __device__ __forceinline__ uint32_t score_key(float r) { return __float_as_uint(r) & 0x7FFFFFFFu; }
