@@ -364,6 +364,12 @@ def run_ours(args, rank, world, local):
                       "issued call by call with events between the calls",
             "eager": {"ms_per_step": round(eager_ms / K, 5), "value": round(retained * K / (eager_ms * 1e-3), 1)},
             "pipeline_frac": round(ideal_s / steps_s, 4),
+            "score_select_compact": {
+                "what": "score, select and compact as one aggregate: their algorithmic bytes over their summed "
+                        "times, against the HBM copy peak",
+                "ms": round(sum(kernels[n]["ms"] for n in ("score", "select", "compact")), 5),
+                "hbm_frac": round(sum(work[n][0] for n in ("score", "select", "compact")) / (pk["hbm"] * 1e9)
+                                  / (sum(kernels[n]["ms"] for n in ("score", "select", "compact")) * 1e-3), 4)},
             "score_to_gemm": {
                 "what": "the metric as its name defines it: retained pairs over the mean time of score, select, "
                         "compact, dgrad and wgrad (route stats reported apart)",
@@ -655,6 +661,23 @@ def cpu_cores():
         return os.cpu_count() or 1
 
 
+def cpu_model():
+    """The host CPU's model name and architecture, as the kernel reports them."""
+    import platform
+
+    model = ""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":", 1)[0].strip().lower()
+                if key in ("model name", "cpu model", "hardware") and ":" in line:
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    return {"model": model or platform.processor() or "unknown", "arch": platform.machine()}
+
+
 def cpu_baseline(inp, tokens, target_s=15.0):
     """The oracle as it stands on a bounded token slice, repeated until about
     `target_s` seconds of timed CPU work have run (at least two passes)."""
@@ -674,7 +697,7 @@ def cpu_baseline(inp, tokens, target_s=15.0):
                       f"{w.name} layer ({sl.workload.N} routed pairs, same E/k/h/I/CF/rho); "
                       f"{steps} timed passes after 1 warm-up; BLAS may use all {cpu_cores()} cores, "
                       "the rest of numpy one",
-            "seconds": round(dt, 3)}
+            "seconds": round(dt, 3), "host": cpu_model()}
 
 
 def run_reference(args, rank, world):
@@ -723,7 +746,8 @@ def run_reference(args, rank, world):
         "data": "synthetic (seeded)",
         "config": {"workload": w.name, "T": w.T, "E": w.E, "k": w.k, "h": w.h, "I": w.I,
                    "sample_tokens": sl.workload.T},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle", "sample": sample,
+                         "host": cpu_model()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
