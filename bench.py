@@ -665,16 +665,24 @@ def cpu_model():
     """The host CPU's model name and architecture, as the kernel reports them."""
     import platform
 
-    model = ""
+    model, impl, part = "", "", ""
     try:
         with open("/proc/cpuinfo") as f:
             for line in f:
-                key = line.split(":", 1)[0].strip().lower()
-                if key in ("model name", "cpu model", "hardware") and ":" in line:
-                    model = line.split(":", 1)[1].strip()
-                    break
+                if ":" not in line:
+                    continue
+                key, val = (x.strip() for x in line.split(":", 1))
+                key = key.lower()
+                if key in ("model name", "cpu model", "hardware") and not model:
+                    model = val
+                elif key == "cpu implementer" and not impl:
+                    impl = val
+                elif key == "cpu part" and not part:
+                    part = val
     except OSError:
         pass
+    if not model and impl:  # Arm cores report an implementer and a part number instead of a name
+        model = f"Arm CPU implementer {impl} part {part}"
     return {"model": model or platform.processor() or "unknown", "arch": platform.machine()}
 
 
