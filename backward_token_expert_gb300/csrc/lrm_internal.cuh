@@ -74,6 +74,19 @@ inline lrm_status launch_status() {
   return e == cudaSuccess ? LRM_OK : LRM_ERR_CUDA;
 }
 
+// Capacity and quota arithmetic, shared by the route-stats kernels and the
+// host queries lrm_capacity / lrm_max_rows.  CF = cf_num / cf_den and
+// rho = rho_num / rho_den are exact rationals with positive denominators.
+// C = floor(CF * N / E).
+__host__ __device__ inline long long capacity_of(long long N, int E, int32_t cf_num, int32_t cf_den) {
+  return (static_cast<long long>(cf_num) * N) / (static_cast<long long>(cf_den) * E);
+}
+// Q = ceil(rho * min(n, C)) for a non-negative count n.
+__host__ __device__ inline long long quota_of(long long n, long long C, int32_t rho_num, int32_t rho_den) {
+  const long long m = n < C ? n : C;
+  return (static_cast<long long>(rho_num) * m + rho_den - 1) / rho_den;
+}
+
 // ---------------------------------------------------------------------------
 // device helpers
 

@@ -200,13 +200,12 @@ __global__ void __launch_bounds__(RR_THREADS) rs_rows(int T, int E, int k, int n
   for (int o = 16; o > 0; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
   if (lane == 0) {
     const int cnt = run;
-    const long long C = (static_cast<long long>(cf_num) * N) / (static_cast<long long>(cf_den) * E);
-    const long long m = cnt < C ? cnt : C;
+    const long long C = capacity_of(N, E, cf_num, cf_den);
     counts[x] = cnt;
     // fp32 throughout: fp64 runs at a small fraction of the fp32 rate on this part
     P[x] = T > 0 ? ps / static_cast<float>(T) : 0.f;
     f[x] = N > 0 ? static_cast<float>(cnt) / static_cast<float>(N) : 0.f;
-    quota[x] = static_cast<int32_t>((static_cast<long long>(rho_num) * m + rho_den - 1) / rho_den);
+    quota[x] = static_cast<int32_t>(quota_of(cnt, C, rho_num, rho_den));
   }
 }
 
@@ -217,7 +216,7 @@ __device__ void write_summary(int T, int E, int k, int32_t cf_num, int32_t cf_de
                               const int32_t* __restrict__ quota, lrm_route_summary* __restrict__ summary) {
   const int lane = threadIdx.x & 31;
   const long long N = static_cast<long long>(T) * k;
-  const long long C = (static_cast<long long>(cf_num) * N) / (static_cast<long long>(cf_den) * E);
+  const long long C = capacity_of(N, E, cf_num, cf_den);
   long long drop = 0, ret = 0, mx = LLONG_MIN, mn = LLONG_MAX, nonempty = 0;
   float fp = 0.f, sp = 0.f;
   for (int e = lane; e < E; e += 32) {
@@ -436,11 +435,52 @@ extern "C" lrm_status lrm_route_stats(lrm_ctx* ctx, const float* logits, const i
                             bucket, P, f, quota, summary, ws_hist, ws_p, s);
 }
 
+// Host queries of the capacity and quota rule, with the kernels' own helpers.
+namespace {
+lrm_status check_rationals(const lrm_dims& dims, int32_t cf_num, int32_t cf_den, int32_t rho_num, int32_t rho_den) {
+  lrm_status st = check_dims(dims);
+  if (st != LRM_OK) return st;
+  if (cf_num <= 0 || cf_den <= 0 || rho_den <= 0 || rho_num < 0 || rho_num > rho_den) return LRM_ERR_INVALID_ARG;
+  return LRM_OK;
+}
+}  // namespace
+
+extern "C" lrm_status lrm_capacity(lrm_dims dims, int32_t cf_num, int32_t cf_den, int32_t* C) {
+  if (C == nullptr) return LRM_ERR_INVALID_ARG;
+  lrm_status st = check_rationals(dims, cf_num, cf_den, 0, 1);
+  if (st != LRM_OK) return st;
+  const long long N = static_cast<long long>(dims.T) * dims.k;
+  const long long c = capacity_of(N, dims.E, cf_num, cf_den);
+  if (c > INT32_MAX / dims.E) return LRM_ERR_SHAPE;  // E * C slots must fit the summary's int32
+  *C = static_cast<int32_t>(c);
+  return LRM_OK;
+}
+
+extern "C" lrm_status lrm_max_rows(lrm_dims dims, int32_t cf_num, int32_t cf_den, int32_t rho_num, int32_t rho_den,
+                                   int32_t* max_rows) {
+  if (max_rows == nullptr) return LRM_ERR_INVALID_ARG;
+  lrm_status st = check_rationals(dims, cf_num, cf_den, rho_num, rho_den);
+  if (st != LRM_OK) return st;
+  const long long N = static_cast<long long>(dims.T) * dims.k;
+  const long long c = capacity_of(N, dims.E, cf_num, cf_den);
+  if (c > INT32_MAX / dims.E) return LRM_ERR_SHAPE;
+  // every quota is at most quota_of(C, C) and at most n_e (sum N); and
+  // ceil(rho m) <= (rho_num m + rho_den - 1) / rho_den summed over E experts
+  long long bound = N;
+  const long long per_expert = quota_of(c, c, rho_num, rho_den) * dims.E;
+  if (per_expert < bound) bound = per_expert;
+  const long long by_rate = (static_cast<long long>(rho_num) * N + static_cast<long long>(dims.E) * (rho_den - 1)) /
+                            rho_den;
+  if (by_rate < bound) bound = by_rate;
+  *max_rows = static_cast<int32_t>(bound);
+  return LRM_OK;
+}
+
 // ---------------------------------------------------------------------------
 // Variant without a caller workspace, for callers that cannot allocate device
 // memory: the scratch of the three kernels is this fixed array.  Host code
 // only sees a stand-in symbol for it, so its device address is looked up
-// once per device (with that device current) and passed to the kernels.
+// with the device current and passed to the kernels.
 
 namespace lrm {
 namespace {
@@ -451,11 +491,18 @@ constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mutex;
 void* g_scratch_addr[kMaxDevices] = {};
 
-// Device address of g_route_stats_scratch on the current device (cached).
-lrm_status scratch_address(int device, void** out) {
+// Device address of g_route_stats_scratch on the current device.  Outside a
+// stream capture it is looked up on every call (a reset of the device's
+// context unloads the module, and the address found before it would be
+// stale); while `stream` is capturing, the address of the last uncaptured
+// call on this device is used, so that the capture records no lookup.
+lrm_status scratch_address(int device, cudaStream_t stream, void** out) {
   if (device < 0 || device >= kMaxDevices) return LRM_ERR_INVALID_ARG;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  const bool capturing = cudaStreamIsCapturing(stream, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone;
+  if (capturing) cudaGetLastError();
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  if (g_scratch_addr[device] == nullptr) {
+  if (!capturing) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_route_stats_scratch) != cudaSuccess || p == nullptr) {
       cudaGetLastError();
@@ -463,6 +510,7 @@ lrm_status scratch_address(int device, void** out) {
     }
     g_scratch_addr[device] = p;
   }
+  if (g_scratch_addr[device] == nullptr) return LRM_ERR_CUDA;  // first call inside a capture
   *out = g_scratch_addr[device];
   return LRM_OK;
 }
@@ -492,9 +540,9 @@ extern "C" lrm_status lrm_route_stats_noalloc(lrm_ctx* ctx, const float* logits,
   if (L.bytes > LRM_ROUTE_STATS_SCRATCH_BYTES) return LRM_ERR_SHAPE;
   DeviceGuard guard(ctx->device);
   if (!guard.ok) return LRM_ERR_CUDA;
-  void* ws = nullptr;
-  if ((st = scratch_address(ctx->device, &ws)) != LRM_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  void* ws = nullptr;
+  if ((st = scratch_address(ctx->device, s, &ws)) != LRM_OK) return st;
   int32_t* ws_hist = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + L.hist_off);
   float* ws_p = reinterpret_cast<float*>(static_cast<char*>(ws) + L.p_off);
   return launch_route_stats(ctx, L, dims, logits, expert_idx, cf_num, cf_den, rho_num, rho_den, counts, offsets,

@@ -61,6 +61,8 @@ EXPORTED = (
     "lrm_zero_dropped_rows",
     "lrm_swiglu_backward",
     "lrm_combine_rows",
+    "lrm_capacity",
+    "lrm_max_rows",
 )
 
 # selection metrics of lrm_score_metric (the ablation of LRMoE sec. 4.7, Table 2)
@@ -141,6 +143,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "lrm_zero_dropped_rows": ([P, P, P, Dims, i32, P, P, ctypes.c_size_t, P], st),
         "lrm_swiglu_backward": ([P, P, P, P, Dims, i32, P, P], st),
         "lrm_combine_rows": ([P, P, P, P, Dims, i32, i32, P, P, ctypes.c_size_t, P], st),
+        "lrm_capacity": ([Dims, i32, i32, ctypes.POINTER(i32)], st),
+        "lrm_max_rows": ([Dims, i32, i32, i32, i32, ctypes.POINTER(i32)], st),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -209,6 +213,24 @@ def lrm_sm_count(ctx: int) -> int:
 def lrm_workspace_size(ctx: int, op: int, dims: Dims) -> int:
     out = ctypes.c_size_t()
     _check(load_library().lrm_workspace_size(ctx, int(op), dims, ctypes.byref(out)), "lrm_workspace_size")
+    return out.value
+
+
+def lrm_capacity(dims: Dims, cf) -> int:
+    """C = floor(CF * N / E), computed by the library (host only)."""
+    cf = Fraction(cf)
+    out = ctypes.c_int32()
+    _check(load_library().lrm_capacity(dims, cf.numerator, cf.denominator, ctypes.byref(out)), "lrm_capacity")
+    return out.value
+
+
+def lrm_max_rows(dims: Dims, cf, rho) -> int:
+    """Upper bound of the retained total over any routing, computed by the library (host only)."""
+    cf = Fraction(cf)
+    rho = Fraction(rho)
+    out = ctypes.c_int32()
+    _check(load_library().lrm_max_rows(dims, cf.numerator, cf.denominator, rho.numerator, rho.denominator,
+                                       ctypes.byref(out)), "lrm_max_rows")
     return out.value
 
 

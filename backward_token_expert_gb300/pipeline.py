@@ -22,23 +22,15 @@ import torch
 from . import lrm as L
 
 
-def capacity(N: int, E: int, cf: Fraction) -> int:
-    """C = floor(CF * N / E) in exact rational arithmetic."""
-    cf = Fraction(cf)
-    return (cf.numerator * N) // (cf.denominator * E)
+def capacity(T: int, E: int, k: int, cf: Fraction) -> int:
+    """C = floor(CF * T k / E), as the library computes it (lrm_capacity)."""
+    return L.lrm_capacity(L.dims_of(T, E, k, 8, 8), cf)
 
 
 def max_retained_rows(T: int, E: int, k: int, cf: Fraction, rho: Fraction) -> int:
-    """Host upper bound of sum_e ceil(rho * min(n_e, C)) over any routing.
-
-    Each quota is at most ceil(rho * C) and at most n_e, so the total is at
-    most min(N, E * ceil(rho * C)).
-    """
-    N = T * k
-    C = capacity(N, E, cf)
-    rho = Fraction(rho)
-    per = -((-rho.numerator * C) // rho.denominator)
-    return max(0, min(N, E * per))
+    """Upper bound of sum_e ceil(rho * min(n_e, C)) over any routing, as the
+    library computes it (lrm_max_rows)."""
+    return L.lrm_max_rows(L.dims_of(T, E, k, 8, 8), cf, rho)
 
 
 @dataclasses.dataclass
@@ -87,8 +79,8 @@ class Recalibration:
         self.device = torch.device("cuda", device) if isinstance(device, int) else torch.device(device)
         self.dims = L.dims_of(T, E, k, h, I)
         self.ctx = L.lrm_create(self.device.index or 0)
-        self.C = capacity(self.N, self.E, self.cf)
-        self.max_rows = max_retained_rows(T, E, k, self.cf, self.rho) if max_rows is None else int(max_rows)
+        self.C = L.lrm_capacity(self.dims, self.cf)
+        self.max_rows = L.lrm_max_rows(self.dims, self.cf, self.rho) if max_rows is None else int(max_rows)
         dev = self.device
         ws_bytes = L.lrm_workspace_size(self.ctx, L.LRM_OP_ROUTE_STATS, self.dims)
         ws_sel = L.lrm_workspace_size(self.ctx, L.LRM_OP_SELECT, self.dims)

@@ -152,6 +152,26 @@ LRM_API lrm_status lrm_route_stats(lrm_ctx* ctx, const float* logits, const int3
                            void* stream);
 
 /*
+ * Host queries of the capacity and quota rule of lrm_route_stats, computed
+ * by the same code the kernels use (no context, no device work, no
+ * allocation; callable without a GPU):
+ *   lrm_capacity  *C = floor(CF * N / E), N = T*k ("Expert Parallel Math
+ *                 Deep", capacity section: capacity is CF times the mean
+ *                 load per expert).
+ *   lrm_max_rows  *max_rows = an upper bound of sum_e Q_e over every routing
+ *                 of the layer, Q_e = ceil(rho * min(n_e, C)) (LRMoE sec. 3.1:
+ *                 quotas with 0 <= Q_e <= n_e): the smallest of N,
+ *                 E * ceil(rho * C) and floor((rho_num N + E (rho_den - 1)) /
+ *                 rho_den).  It sizes sel_ids and the compacted buffers.
+ * CF = cf_num / cf_den and rho = rho_num / rho_den as for lrm_route_stats.
+ * Errors: LRM_ERR_INVALID_ARG (null output, bad rational), the dims checks
+ * of every call, LRM_ERR_SHAPE if E * C does not fit in int32.
+ */
+LRM_API lrm_status lrm_capacity(lrm_dims dims, int32_t cf_num, int32_t cf_den, int32_t* C);
+LRM_API lrm_status lrm_max_rows(lrm_dims dims, int32_t cf_num, int32_t cf_den, int32_t rho_num, int32_t rho_den,
+                                int32_t* max_rows);
+
+/*
  * Step 2 - the Load Recalibration Metric (LRMoE sec. 3.2 Prop. 3.1 eq. (3);
  * Alg. 1): score[u] = alpha[u]^2 * ||g_t||^2 * ||phi_u||^2, the
  * squared Frobenius norm of the rank-one gradient contribution
@@ -347,9 +367,13 @@ LRM_API lrm_status lrm_compact_padded(lrm_ctx* ctx, const uint16_t* delta_c, con
  *   work.  Every entry is written before it is read, so nothing in the
  *   scratch has to start at zero and stale contents of an earlier call are
  *   harmless.
- * - The first call on a device looks up the array's device address (with
- *   that device current) and caches it; make that first call before any
- *   stream capture.
+ * - Every call looks up the array's device address with the device current
+ *   (host-side, no device work).  A call made while `stream` is being
+ *   captured into a CUDA graph reuses the address found by the last call on
+ *   that device outside a capture: make one call before capturing, and one
+ *   more after any reset of the device (cudaDeviceReset) before capturing
+ *   again.  A capture whose first call on the device is this one fails with
+ *   LRM_ERR_CUDA.
  * - All calls share the one array, so calls that may overlap on the GPU
  *   (different streams without ordering between them) race; serialise them.
  * The paper has no counterpart of this entry point.

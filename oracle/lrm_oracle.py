@@ -49,6 +49,7 @@ __all__ = [
     "round_f64_to_bf16",
     "softmax_rows",
     "route_stats",
+    "capacity_and_quotas",
     "aux_loss",
     "score",
     "score_metric",
@@ -125,6 +126,18 @@ def _ceil_div(a, b):
     return -((-a) // b)
 
 
+def capacity_and_quotas(counts, N: int, E: int, cf=Fraction(5, 4), rho=Fraction(3, 4)):
+    """C = floor(CF * N / E) in exact rationals (EPM, capacity section) and
+    the quotas Q_e = ceil(rho * min(n_e, C)) of the routed counts n_e (LRMoE
+    sec. 3.1 quotas, under the quota rule read above).  Returns (C, Q)."""
+    cf = Fraction(cf)
+    rho = Fraction(rho)
+    C = (cf.numerator * N) // (cf.denominator * E)
+    m = np.minimum(np.asarray(counts, dtype=np.int64), C)
+    Q = _ceil_div(rho.numerator * m, rho.denominator).astype(np.int64)
+    return C, Q
+
+
 def route_stats(logits, expert_idx, E: int, cf=Fraction(5, 4), rho=Fraction(3, 4), quota=None):
     """Per-expert routing statistics, capacity, drop rate and retention quotas.
 
@@ -160,14 +173,11 @@ def route_stats(logits, expert_idx, E: int, cf=Fraction(5, 4), rho=Fraction(3, 4
     f = counts.astype(np.float64) / N
     aux = aux_loss(f, P)
 
-    cf = Fraction(cf)
-    rho = Fraction(rho)
-    C = (cf.numerator * N) // (cf.denominator * E)
+    C, Q_rule = capacity_and_quotas(counts, N, E, cf, rho)
     over = np.maximum(counts - C, 0)
     dropped = int(over.sum())
     if quota is None:
-        m = np.minimum(counts, C)
-        Q = _ceil_div(rho.numerator * m, rho.denominator).astype(np.int64)
+        Q = Q_rule
     else:
         Q = np.asarray(quota, dtype=np.int64).copy()
         if Q.shape != (E,) or np.any(Q < 0) or np.any(Q > counts):

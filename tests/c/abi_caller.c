@@ -8,7 +8,9 @@
  *                               select, compact, dgrad and wgrad on stream 0,
  *                               write the results to <out>
  *
- * <in>:  int32 T, E, k, h, I, cf_num, cf_den, rho_num, rho_den, max_rows; then
+ * <in>:  int32 T, E, k, h, I, cf_num, cf_den, rho_num, rho_den, max_rows (the
+ *        caller's expectation; the program sizes its buffers with lrm_max_rows
+ *        and fails if the two differ); then
  *        logits f32[T*E], expert_idx i32[T*k], alpha f32[T*k], g bf16[T*h],
  *        phi bf16[T*k*I], W bf16[E*h*I]
  * <out>: uint32 device status; f32 score[T*k]; int32 sel_offsets[E+1],
@@ -74,7 +76,12 @@ int main(int argc, char** argv) {
   int32_t hdr[10];
   if (fread(hdr, sizeof(int32_t), 10, in) != 10) return 1;
   const lrm_dims dims = {hdr[0], hdr[1], hdr[2], hdr[3], hdr[4]};
-  const int32_t max_rows = hdr[9];
+  int32_t max_rows = 0;
+  CHECK_LRM(lrm_max_rows(dims, hdr[5], hdr[6], hdr[7], hdr[8], &max_rows));
+  if (max_rows != hdr[9]) {
+    fprintf(stderr, "lrm_max_rows gave %d, the input expects %d\n", (int)max_rows, (int)hdr[9]);
+    return 4;
+  }
   const size_t T = (size_t)dims.T, E = (size_t)dims.E, k = (size_t)dims.k, h = (size_t)dims.h, I = (size_t)dims.I;
   const size_t N = T * k;
   void* h_logits = read_block(in, T * E * 4);

@@ -13,7 +13,7 @@ import pytest
 
 from backward_token_expert_gb300 import build as B
 from backward_token_expert_gb300 import lrm as L
-from backward_token_expert_gb300.pipeline import capacity, max_retained_rows
+import oracle as O
 
 HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "lrm.h")
 
@@ -80,19 +80,49 @@ def test_python_wrapper_raises_on_error(lib):
     assert ei.value.code == L.LRM_ERR_INVALID_ARG
 
 
-def test_capacity_and_row_bound():
-    assert capacity(131072, 8, Fraction(5, 4)) == 20480
-    assert capacity(262144, 128, Fraction(5, 4)) == 2560
+def test_capacity_query_matches_the_oracle_on_the_worked_example(lib, golden):
+    # "Expert Parallel Math Deep" worked example: 8 experts, T k = 131072 routed
+    # pairs, CF = 1.25 -> C = 20480; the oracle's C is the pin
+    ex = golden("expert_parallel_math_worked_example.json")
+    loads = np.asarray(ex["loads"], dtype=np.int64)
+    E, N = loads.size, int(loads.sum())
+    cf = Fraction(*ex["CF"])
+    T, k = N // 2, 2
+    ids = np.repeat(np.arange(E), loads)
+    idx = np.stack([ids[:T], ids[T:]], axis=1)
+    st = O.route_stats(np.zeros((T, E)), idx, E, cf, Fraction(3, 4))
+    dims = L.dims_of(T, E, k, 8, 8)
+    assert L.lrm_capacity(dims, cf) == st["C"] == ex["C"]
+    assert st["retained"] <= L.lrm_max_rows(dims, cf, Fraction(3, 4))
+    assert L.lrm_capacity(L.dims_of(32768, 128, 8, 2048, 768), Fraction(5, 4)) == 2560
+
+
+def test_row_bound_covers_every_routing_and_is_reached(lib):
     rng = np.random.default_rng(0)
-    for _ in range(200):
+    reached = 0
+    for _ in range(300):
         E = int(rng.integers(1, 20))
         k = int(rng.integers(1, E + 1))
-        T = int(rng.integers(0, 200))
+        T = int(rng.integers(1, 200))
         cf = Fraction(int(rng.integers(1, 9)), int(rng.integers(1, 5)))
         rho = Fraction(int(rng.integers(0, 5)), 4)
-        p = rng.dirichlet(np.ones(E) * 0.3)
-        idx = np.stack([rng.choice(E, size=k, replace=False, p=p) for _ in range(T)]) if T else np.zeros((0, k))
-        n = np.bincount(idx.reshape(-1).astype(int), minlength=E)
-        C = capacity(T * k, E, cf)
-        Q = [-((-rho.numerator * min(int(c), C)) // rho.denominator) for c in n]
-        assert sum(Q) <= max_retained_rows(T, E, k, cf, rho)
+        p = rng.dirichlet(np.ones(E) * (0.3 if rng.random() < 0.7 else 50.0))
+        idx = np.stack([rng.choice(E, size=k, replace=False, p=p) for _ in range(T)])
+        st = O.route_stats(np.zeros((T, E)), idx, E, cf, rho)
+        dims = L.dims_of(T, E, k, 8, 8)
+        assert L.lrm_capacity(dims, cf) == st["C"]
+        bound = L.lrm_max_rows(dims, cf, rho)
+        assert st["retained"] <= bound
+        reached += st["retained"] == bound
+    assert reached > 0  # the bound is tight for some routings
+
+
+def test_capacity_queries_reject_bad_arguments(lib):
+    d = L.dims_of(16, 4, 2, 64, 32)
+    out = ctypes.c_int32()
+    assert lib.lrm_capacity(d, 5, 4, None) == L.LRM_ERR_INVALID_ARG
+    assert lib.lrm_capacity(d, 0, 4, ctypes.byref(out)) == L.LRM_ERR_INVALID_ARG
+    assert lib.lrm_max_rows(d, 5, 4, 5, 4, ctypes.byref(out)) == L.LRM_ERR_INVALID_ARG  # rho > 1
+    assert lib.lrm_max_rows(L.dims_of(16, 4, 2, 60, 32), 5, 4, 3, 4, ctypes.byref(out)) == L.LRM_ERR_ALIGN
+    # E * C beyond int32
+    assert lib.lrm_capacity(L.dims_of(1 << 20, 2, 2, 8, 8), 1 << 30, 1, ctypes.byref(out)) == L.LRM_ERR_SHAPE

@@ -10,6 +10,7 @@ import pytest
 
 import oracle as O
 from gpu_common import (
+    GEMM_RTOL,
     SCORE_RTOL,
     built_library,
     check_compaction,
@@ -18,9 +19,10 @@ from gpu_common import (
     check_selection,
     need_gpu,
     rel_close,
+    rel_fro,
     run_gpu,
 )
-from workloads import generate
+from workloads import generate, get_workload
 
 pytestmark = pytest.mark.gpu
 
@@ -31,10 +33,60 @@ def _setup():
     built_library()
 
 
-def sampled_check(name, n_pairs=20000, n_rows=4096, n_random_experts=3):
-    inp = generate(name)
+_SHARED = {}
+
+
+def sweep_inputs(name):
+    """The sweep points share one seed, so their g, phi and W are the same
+    arrays: draw them once and only redo the routing of each point."""
+    from workloads.generate import Inputs
+
+    w = get_workload(name)
+    if "base" not in _SHARED:
+        _SHARED["base"] = generate(w)
+    base = _SHARED["base"]
+    r = generate(w, parts=())
+    return Inputs(w, r.logits, r.expert_idx, r.alpha, base.g, base.phi, base.W, r.bias)
+
+
+def check_padded(gpu, inp, so, ids, experts):
+    """The zero-masked comparator (LRMoE sec. 3.4): every expert's slots hold
+    its compacted rows then zeros (in full, bit for bit), the sampled experts'
+    rows equal the oracle's compaction, and the GEMMs on the padded buffers
+    match the oracle (sampled experts) and the compacted GEMMs (all experts)."""
     w = inp.workload
-    gpu = run_gpu(inp)
+    C = gpu["C"]
+    assert np.array_equal(gpu["pad_offsets"], np.arange(w.E + 1) * C)
+    dpad = gpu["delta_pad"].reshape(w.E, C, w.h)
+    ppad = gpu["phi_pad"].reshape(w.E, C, w.I)
+    dphi_pad = gpu["dphi_pad"].reshape(w.E, C, w.I)
+    for e in range(w.E):
+        q = int(so[e + 1] - so[e])
+        assert q <= C
+        assert np.array_equal(dpad[e, :q], gpu["delta_c"][so[e]:so[e + 1]]), e
+        assert np.array_equal(ppad[e, :q], gpu["phi_c"][so[e]:so[e + 1]]), e
+        assert not dpad[e, q:].any() and not ppad[e, q:].any() and not dphi_pad[e, q:].any(), e
+        ref = gpu["dW"][e].astype(np.float64)
+        if q == 0:
+            assert not gpu["dW_pad"][e].any()
+        else:
+            assert np.linalg.norm(gpu["dW_pad"][e] - ref) <= 1e-5 * np.linalg.norm(ref), e
+    ref_dW = O.grouped_wgrad(inp.g, inp.phi, inp.alpha, so, ids, w.E, w.k, experts)
+    ref_dphi = O.grouped_dgrad(inp.g, inp.W, inp.alpha, so, ids, w.E, w.k, experts)
+    for e in experts:
+        q = int(so[e + 1] - so[e])
+        if q == 0:
+            continue
+        dc, pc, _ = O.compact(inp.g, inp.phi, inp.alpha, ids[so[e]:so[e + 1]], w.k)
+        assert np.array_equal(dpad[e, :q], dc) and np.array_equal(ppad[e, :q], pc), e
+        assert rel_fro(gpu["dW_pad"][e], ref_dW[e]) <= GEMM_RTOL, e
+        assert rel_fro(O.bf16_to_f64(dphi_pad[e, :q]), ref_dphi[e]) <= GEMM_RTOL, e
+
+
+def sampled_check(name, n_pairs=20000, n_rows=4096, n_random_experts=3, inp=None, padded=False):
+    inp = generate(name) if inp is None else inp
+    w = inp.workload
+    gpu = run_gpu(inp, padded=padded)
     st = O.route_stats(inp.logits, inp.expert_idx, w.E, w.cf, w.rho)
     check_route_stats(gpu, inp, st)
     assert np.array_equal(gpu["quota"], st["quota"])
@@ -58,6 +110,8 @@ def sampled_check(name, n_pairs=20000, n_rows=4096, n_random_experts=3):
     experts.update(int(e) for e in rng.choice(nz, size=min(n_random_experts, nz.size), replace=False))
     experts.update(int(e) for e in np.flatnonzero(q == 0))  # exact zeros
     worst = check_gemms(gpu, inp, so, ids, sorted(experts))
+    if padded:
+        check_padded(gpu, inp, so, ids, sorted(experts))
     return inp, gpu, st, worst
 
 
@@ -83,9 +137,16 @@ def test_glm45_air_layer():
     sampled_check("glm45_air_T32768_E128_k8_h4096_I1408")
 
 
-def test_skew_sweep_corners():
-    sampled_check("qwen3_sweep_s0_rho1_1", n_random_experts=2)
-    sampled_check("qwen3_sweep_s1.6_rho1_2", n_random_experts=2)
+SWEEP = [f"qwen3_sweep_s{s:g}_rho{r}" for s in (0.0, 0.8, 1.2, 1.6) for r in ("1_1", "3_4", "1_2")]
+
+
+@pytest.mark.parametrize("name", SWEEP)
+def test_skew_sweep_point_with_zero_masked_comparator(name):
+    # every point of the skew / retention sweep (Zipf s x rho on the
+    # Qwen3-shaped layer): the compacted path and the capacity-padded
+    # comparator that is timed against it on the same tensors
+    inp, gpu, st, _ = sampled_check(name, n_random_experts=2, inp=sweep_inputs(name), padded=True)
+    assert gpu["summary"]["retained"] == st["retained"]
 
 
 def test_large_batch_stress_with_empty_and_oversized_experts():

@@ -53,9 +53,13 @@ def test_noalloc_route_stats_matches_workspace_version_twice():
     dev = "cuda:0"
     ctx = L.lrm_create(0)
     try:
+        # calls in a row on one array: the second reuses what the first left, and
+        # the third, a small layer with other E and k after the large one, reads
+        # a scratch whose earlier contents span more blocks and another row pitch
         cases = [custom_inputs(T=3000, E=16, k=4, h=64, I=32, s=1.0, rho=Fraction(3, 4), seed=31),
-                 custom_inputs(T=32768, E=128, k=8, h=64, I=32, s=0.8, rho=Fraction(3, 4), seed=32)]
-        for inp in cases:  # two calls in a row; the second reuses the scratch of the first
+                 custom_inputs(T=32768, E=128, k=8, h=64, I=32, s=0.8, rho=Fraction(3, 4), seed=32),
+                 custom_inputs(T=700, E=24, k=3, h=64, I=32, s=1.2, rho=Fraction(1, 2), seed=33, dead=2)]
+        for inp in cases:
             w = inp.workload
             dims = L.dims_of(w.T, w.E, w.k, w.h, w.I)
             logits = torch.from_numpy(inp.logits).to(dev)
