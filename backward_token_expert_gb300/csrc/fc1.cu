@@ -1,6 +1,6 @@
 // FC1 side of the expert backward on the retained pairs (LRMoE sec. 3.4:
-// compaction reduces the row dimension of all four expert-backward GEMMs,
-// FC1 and FC2 data- and weight-gradient).  The activation is read as SwiGLU:
+// the compacted row count is the M or K of every expert-backward GEMM, the
+// input- and weight-gradient products of both FC1 and FC2).  The activation is read as SwiGLU:
 // FC1 gives [a | b] (gate, up; width 2I) and the FC2 input is
 // phi = silu(a) * b.  The two FC1 GEMMs are the grouped dgrad / wgrad kernels
 // with the dimensions relabelled (K = 2I); this file holds the two pieces

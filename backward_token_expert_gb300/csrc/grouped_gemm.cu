@@ -1,9 +1,8 @@
 // Step 5 of the path: the packed expert backward of FC2 as variable-size
-// grouped GEMMs without padding (LRMoE sec. 3.3: "m determines the row
-// dimension of input-gradient products and the reduction dimension of
-// weight-gradient products, while parameter dimensions remain unchanged";
-// sec. 3.4 and Fig. 4: variable M, no padding rows; appendix 7.1 eq. (6),
-// (8), (9)).  With the compacted, expert-major rows of step 4:
+// grouped GEMMs without padding (LRMoE sec. 3.3: the number of kept rows of
+// an expert is the M of its input-gradient product and the K of its
+// weight-gradient product, and the weight shapes do not change; sec. 3.4 and
+// Fig. 4: variable M, no padding rows; appendix 7.1 eq. (6), (8), (9)).  With the compacted, expert-major rows of step 4:
 //   dgrad  dphi_c[seg e] = delta_c[seg e] . W_e      M = Q_e (ragged), N = I, K = h
 //   wgrad  dW_e          = delta_c[seg e]^T . phi_c  M = h, N = I, K = Q_e (ragged)
 //

@@ -1,6 +1,7 @@
-// The inverse mapping of LRMoE (sec. 1 and 3.3; Alg. 1,
-// ScatterWithZeros; sec. 3.4: the retained results go back to their original
-// positions and zeros are restored before the next dense-layer boundary).
+// The inverse mapping of LRMoE (sec. 1 and 3.3; Alg. 1, ScatterWithZeros;
+// sec. 3.4): every kept row returns to the slot its pair had before
+// compaction, and the slots of dropped pairs are filled with zeros so that
+// the next dense layer sees the layout it expects.
 // lrm_grouped_dgrad_scatter writes every retained row of the input gradient
 // to its pair's row; this file zeroes the rows of the pairs that were not
 // retained.  Two launches:

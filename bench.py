@@ -55,6 +55,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-comparator", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip the other layers and the comparator sweep")
+    ap.add_argument("--cpu-steps-child", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--ref-tokens", type=int, default=0, help="token slice of the reference arm's step")
     return ap.parse_args()
 
@@ -173,9 +175,13 @@ def algorithmic_work(w, retained, active_experts):
     }
 
 
-def roofline_entry(nbytes, flop, ms, pk, sustained):
+def roofline_entry(nbytes, flop, ms, pk):
+    """Roofline of one kernel from its mean per-call CUDA-event time.  Every
+    such time is of a single launch well under a millisecond, so the tensor
+    roof is the burst bf16 peak (the sustained one applies to seconds-long
+    loops of one GEMM under the power cap)."""
     t_hbm = nbytes / (pk["hbm"] * 1e9)
-    tc_peak = pk["bf16_sustained"] if sustained else pk["bf16"]
+    tc_peak = pk["bf16"]
     t_tc = flop / (tc_peak * 1e12)
     sec = ms * 1e-3
     if t_tc > t_hbm:
@@ -215,67 +221,66 @@ def measured_traffic(kernel):
 # our arm
 
 
-def run_ours(args, rank, world, local):
+def issue_step(rec, d, ev=None, stream=None):
+    """One step issued call by call; with `ev` (seven CUDA events) an event is
+    recorded before the first and after every kernel call."""
+    if ev is None:
+        rec.run(d["logits"], d["expert_idx"], d["g"], d["phi"], d["alpha"], d["W"])
+        return
+    calls = (lambda: rec.route_stats(d["logits"], d["expert_idx"]), lambda: rec.score(d["g"], d["phi"], d["alpha"]),
+             rec.select, lambda: rec.compact(d["g"], d["phi"], d["alpha"]), lambda: rec.dgrad(d["W"]), rec.wgrad)
+    ev[0].record(stream)
+    for i, call in enumerate(calls):
+        call()
+        ev[i + 1].record(stream)
+
+
+def per_kernel_times(rec, d, K):
+    """Per-kernel CUDA-event times (ms) of K steps issued call by call, and
+    the eager step time."""
     import torch
 
-    from backward_token_expert_gb300 import build as B
-    from backward_token_expert_gb300.pipeline import Recalibration, StepGraph, to_device_inputs
-    from backward_token_expert_gb300.replicas import job_totals, replica_seed
-    from workloads import generate, get_workload
-
-    torch.cuda.set_device(local)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    if rank == 0:
-        B.build()
-    if dist:
-        dist.barrier()
-
-    # independent replicas: rank r draws its own layer batch
-    w = get_workload(args.workload, seed=replica_seed(rank))
-    inp = generate(w)
-    rec = Recalibration(w.T, w.E, w.k, w.h, w.I, w.cf, w.rho, device=local)
-    d = to_device_inputs(inp, f"cuda:{local}")
     stream = torch.cuda.current_stream()
-
-    def step(ev=None):
-        if ev is None:
-            rec.run(d["logits"], d["expert_idx"], d["g"], d["phi"], d["alpha"], d["W"])
-            return
-        ev[0].record(stream)
-        rec.route_stats(d["logits"], d["expert_idx"])
-        ev[1].record(stream)
-        rec.score(d["g"], d["phi"], d["alpha"])
-        ev[2].record(stream)
-        rec.select()
-        ev[3].record(stream)
-        rec.compact(d["g"], d["phi"], d["alpha"])
-        ev[4].record(stream)
-        rec.dgrad(d["W"])
-        ev[5].record(stream)
-        rec.wgrad()
-        ev[6].record(stream)
-
-    for _ in range(max(3, args.warmup)):
-        step()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(K)]
     torch.cuda.synchronize()
-    flags = rec.device_status()
-    if flags:
-        raise RuntimeError(f"device status flags {flags:#x}")
-    summ = rec.summary()
-    retained = int(summ["retained"])
+    for i in range(K):
+        issue_step(rec, d, evs[i], stream)
+    torch.cuda.synchronize()
+    eager_ms = evs[0][0].elapsed_time(evs[-1][6])
+    per = {name: [evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K)] for j, name in enumerate(KERNELS)}
+    return per, eager_ms
 
-    # the timed steps: the whole step as one CUDA graph (StepGraph), replayed
+
+def kernel_table(w, retained, active, per, pk):
+    """Per-kernel mean time, percentiles, share of the step and roofline."""
+    work = algorithmic_work(w, retained, active)
+    total = sum(sum(v) for v in per.values())
+    kernels = {}
+    for name in KERNELS:
+        ms = statistics.mean(per[name])
+        nbytes, flop = work[name]
+        ent = roofline_entry(nbytes, flop, ms, pk)
+        q = np.percentile(per[name], [10, 50, 90])
+        ent.update(ms=round(ms, 5), ms_p10=round(float(q[0]), 5), ms_median=round(float(q[1]), 5),
+                   ms_p90=round(float(q[2]), 5), share=round(sum(per[name]) / total, 4))
+        kernels[name] = ent
+    return kernels, work
+
+
+def graph_steps(rec, d, K, sampler=None, dist=None):
+    """K whole steps replayed as one CUDA graph, timed with CUDA events on the
+    current stream with a synchronize (and a barrier under torchrun) on both
+    sides; returns (total ms, host seconds)."""
+    import torch
+
+    from backward_token_expert_gb300.pipeline import StepGraph
+
     graph = StepGraph(rec, d["logits"], d["expert_idx"], d["g"], d["phi"], d["alpha"], d["W"])
     for _ in range(3):
         graph.replay()
     torch.cuda.synchronize()
-    K = args.steps
+    stream = torch.cuda.current_stream()
     e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    sampler = ClockSampler(local) if rank == 0 else None
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
@@ -293,19 +298,61 @@ def run_ours(args, rank, world, local):
         sampler.stop()
     if dist:
         dist.barrier()
-    total_ms = e_start.elapsed_time(e_end)
+    return e_start.elapsed_time(e_end), t_host
+
+
+def prepare_layer(w, inp, local, warmup):
+    """Device inputs and buffers of one layer, warmed up and checked."""
+    import torch
+
+    from backward_token_expert_gb300.pipeline import Recalibration, to_device_inputs
+
+    rec = Recalibration(w.T, w.E, w.k, w.h, w.I, w.cf, w.rho, device=local)
+    d = to_device_inputs(inp, f"cuda:{local}")
+    for _ in range(max(3, warmup)):
+        issue_step(rec, d)
+    torch.cuda.synchronize()
+    flags = rec.device_status()
+    if flags:
+        raise RuntimeError(f"device status flags {flags:#x} on {w.name}")
+    return rec, d
+
+
+def run_ours(args, rank, world, local):
+    import torch
+
+    from backward_token_expert_gb300 import build as B
+    from backward_token_expert_gb300.replicas import job_totals, replica_seed
+    from workloads import generate, get_workload
+
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    if rank == 0:
+        B.build()
+    if dist:
+        dist.barrier()
+
+    # independent replicas: rank r draws its own layer batch
+    w = get_workload(args.workload, seed=replica_seed(rank))
+    inp = generate(w)
+    rec, d = prepare_layer(w, inp, local, args.warmup)
+    summ = rec.summary()
+    retained = int(summ["retained"])
+
+    # the timed steps: the whole step as one CUDA graph (StepGraph), replayed
+    K = args.steps
+    sampler = ClockSampler(local) if rank == 0 else None
+    total_ms, t_host = graph_steps(rec, d, K, sampler, dist)
     # whole job: pairs of every replica over the slowest replica's time
     job_pairs, job_s = job_totals(retained * K, total_ms * 1e-3, device=f"cuda:{local}")
     total_ms = job_s * 1e3
 
     # per-kernel times: the same step issued call by call, events between the calls
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(K)]
-    torch.cuda.synchronize()
-    for i in range(K):
-        step(evs[i])
-    torch.cuda.synchronize()
-    eager_ms = evs[0][0].elapsed_time(evs[-1][6])
-    per = {name: [evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K)] for j, name in enumerate(KERNELS)}
+    per, eager_ms = per_kernel_times(rec, d, K)
     flags = rec.device_status()
     if flags:
         raise RuntimeError(f"device status flags {flags:#x} after the timed steps")
@@ -315,29 +362,18 @@ def run_ours(args, rank, world, local):
         pk = peaks()
         so = rec.buf.sel_offsets.cpu().numpy()
         active = int((np.diff(so) > 0).sum())
-        work = algorithmic_work(w, retained, active)
-        kernels = {}
-        for name in KERNELS:
-            ms = statistics.mean(per[name])
-            nbytes, flop = work[name]
-            ent = roofline_entry(nbytes, flop, ms, pk, sustained=True)
-            q = np.percentile(per[name], [10, 50, 90])
-            ent.update(ms=round(ms, 5), ms_p10=round(float(q[0]), 5), ms_median=round(float(q[1]), 5),
-                       ms_p90=round(float(q[2]), 5),
-                       share=round(sum(per[name]) / sum(sum(v) for v in per.values()), 4))
-            kernels[name] = ent
+        kernels, work = kernel_table(w, retained, active, per, pk)
         dominant = max(KERNELS, key=lambda n: kernels[n]["ms"])
         top = {k2: kernels[dominant][k2] for k2 in ("bound", "achieved", "peak", "unit", "frac")}
         top.update(kernel=dominant, traffic=measured_traffic(dominant) if w.name == DEFAULT_WORKLOAD else None,
                    algorithmic_bytes=kernels[dominant]["bytes"],
-                   peak_kind="sustained bf16 (of measured)" if top["bound"] == "tensor" else "hbm copy (of measured)",
+                   peak_kind="burst bf16 (of measured)" if top["bound"] == "tensor" else "hbm copy (of measured)",
                    peak_source=pk["source"])
         value = job_pairs / job_s
         in_bytes = w.N * w.I * 2 + w.E * w.h * w.I * 2 + w.T * w.h * 2
         # pipeline fraction: the time every step would take at its binding roof,
         # over the measured time of the steps
-        ideal_s = sum(max(work[n][0] / (pk["hbm"] * 1e9), work[n][1] / (pk["bf16_sustained"] * 1e12))
-                      for n in KERNELS)
+        ideal_s = sum(max(work[n][0] / (pk["hbm"] * 1e9), work[n][1] / (pk["bf16"] * 1e12)) for n in KERNELS)
         steps_s = sum(kernels[n]["ms"] for n in KERNELS) * 1e-3
         excl_rs_s = sum(kernels[n]["ms"] for n in KERNELS if n != "route_stats") * 1e-3
         result = {
@@ -396,13 +432,112 @@ def run_ours(args, rank, world, local):
         ent = e2e(rec, inp, w, retained, min(K, 20), local)
         if result is not None:
             result["e2e"] = ent
+    rec.close()
+    del rec, d
+    if result is not None and not args.no_configs:
+        # the other layers of the scope, each with its own timed steps and clocks
+        torch.cuda.empty_cache()
+        result["comparator_sweep"] = comparator_sweep(local, peaks())
+        result["configs"] = {}
+        for name in OTHER_CONFIGS:
+            result["configs"][name] = other_config(name, local, min(K, 20), args.warmup, peaks())
     if result is not None and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(inp, tokens=args.ref_tokens or 8192)
-    rec.close()
+        result["cpu_baseline"]["per_step"] = cpu_per_step(inp.workload.name, tokens=4096)
     if dist:
         dist.barrier()
         dist.destroy_process_group()
     return result
+
+
+# the layers measured next to the headline one (configs of the scope besides
+# the tiny one and the sweep)
+OTHER_CONFIGS = ("glm45_air_T32768_E128_k8_h4096_I1408", "stress_T131072_E128_k8_h4096_I1408",
+                 "deepseek_v2_T32768_E160_k6_h5120_I1536")
+
+
+def other_config(name, local, K, warmup, pk):
+    """The step on another layer: graph-replayed steps with clocks sampled
+    during them, and per-kernel times with their rooflines."""
+    import torch
+
+    from workloads import generate, get_workload
+
+    w = get_workload(name)
+    inp = generate(w)
+    rec, d = prepare_layer(w, inp, local, warmup)
+    del inp
+    try:
+        summ = rec.summary()
+        retained = int(summ["retained"])
+        sampler = ClockSampler(local)
+        total_ms, _ = graph_steps(rec, d, K, sampler)
+        per, _ = per_kernel_times(rec, d, K)
+        flags = rec.device_status()
+        if flags:
+            raise RuntimeError(f"device status flags {flags:#x} on {name}")
+        so = rec.buf.sel_offsets.cpu().numpy()
+        kernels, _ = kernel_table(w, retained, int((np.diff(so) > 0).sum()), per, pk)
+        return {
+            "value": round(retained * K / (total_ms * 1e-3), 1), "unit": UNIT, "ms_per_step": round(total_ms / K, 5),
+            "steps": K, "retained_pairs": retained, "routed_pairs": w.N, "C": summ["C"],
+            "max_over_mean": round(summ["max_over_mean"], 3), "empty_experts": w.E - summ["nonempty"],
+            "experts_over_C": int((rec.buf.counts > summ["C"]).sum().item()),
+            "kernels": {n: {k2: kernels[n][k2] for k2 in ("ms", "bound", "achieved", "unit", "frac", "hbm_frac")
+                            + (("tensor_frac",) if "tensor_frac" in kernels[n] else ())} for n in KERNELS},
+            "clocks": sampler.summary(),
+        }
+    finally:
+        rec.close()
+        del rec, d
+        torch.cuda.empty_cache()
+
+
+def comparator_sweep(local, pk, iters=10):
+    """Compacted GEMMs against the zero-masked capacity-padded ones at every
+    point of the skew / retention sweep, on identical tensors (the sweep
+    points share one seed, so g, phi and W are drawn and uploaded once)."""
+    import torch
+
+    from backward_token_expert_gb300.pipeline import to_device_inputs
+    from workloads import generate, get_workload
+    from workloads.generate import Inputs
+
+    names = [f"qwen3_sweep_s{s:g}_rho{r}" for s in (0.0, 0.8, 1.2, 1.6) for r in ("1_1", "3_4", "1_2")]
+    base = generate(get_workload(names[0]))
+    shared = None
+    points = {}
+    for name in names:
+        w = get_workload(name)
+        r = generate(w, parts=())
+        inp = Inputs(w, r.logits, r.expert_idx, r.alpha, base.g, base.phi, base.W, r.bias)
+        if shared is None:
+            shared = to_device_inputs(inp, f"cuda:{local}")
+            d = shared
+        else:
+            d = dict(shared, logits=torch.from_numpy(r.logits).to(shared["g"].device),
+                     expert_idx=torch.from_numpy(r.expert_idx).to(shared["g"].device),
+                     alpha=torch.from_numpy(r.alpha).to(shared["g"].device))
+        from backward_token_expert_gb300.pipeline import Recalibration
+
+        rec = Recalibration(w.T, w.E, w.k, w.h, w.I, w.cf, w.rho, device=local)
+        try:
+            issue_step(rec, d)
+            torch.cuda.synchronize()
+            summ = rec.summary()
+            ent = comparator(rec, d, w, int(summ["retained"]), pk, iters=iters)
+            ent.update(zipf_s=w.zipf_s, rho=str(w.rho), retained_pairs=int(summ["retained"]),
+                       max_over_mean=round(summ["max_over_mean"], 3))
+            for key in ("what", "padded_slots"):
+                ent.pop(key, None)
+            points[name] = ent
+        finally:
+            rec.close()
+    del shared
+    torch.cuda.empty_cache()
+    return {"what": "compact+dgrad+wgrad on the retained rows vs compact_padded+dgrad+wgrad at M=C per expert "
+                    "(E*C = 327680 slots), same kernels and tensors, every (zipf s, rho) point",
+            "points": points}
 
 
 def bf16_dw_step(rec, d, w, retained, pk, work, iters):
@@ -431,7 +566,7 @@ def bf16_dw_step(rec, d, w, retained, pk, work, iters):
     if flags:
         raise RuntimeError(f"device status flags {flags:#x} in the bf16-dW step")
     nbytes = work["wgrad"][0] - 2 * w.E * w.h * w.I
-    ent = roofline_entry(nbytes, work["wgrad"][1], out["wgrad_ms"], pk, sustained=True)
+    ent = roofline_entry(nbytes, work["wgrad"][1], out["wgrad_ms"], pk)
     return {"what": "the timed step (CUDA graph) with dW stored as bf16",
             "value": round(retained / (out["step_ms"] * 1e-3), 1), "unit": UNIT,
             "ms_per_step": round(out["step_ms"], 5), "steps": iters,
@@ -518,7 +653,7 @@ def fc1_backward(rec, w, retained, pk, iters=20):
         e1.record(s)
         e1.synchronize()
         ms = e0.elapsed_time(e1) / iters
-        out[name] = dict(ms=round(ms, 5), **roofline_entry(nbytes, flop, ms, pk, sustained=False))
+        out[name] = dict(ms=round(ms, 5), **roofline_entry(nbytes, flop, ms, pk))
     for _ in range(3):
         rec.fc1_backward(x, ab, W1)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -578,6 +713,7 @@ def comparator(rec, d, w, retained, pk, iters=20):
         algorithmic_flop=flops_alg, padded_flop=flops_pad, padded_slots=E * C,
         speedup=round(out["zero_masked_ms"] / out["compacted_ms"], 3),
         zero_masked_algorithmic_tflops=round(flops_alg / (out["zero_masked_ms"] * 1e-3) / 1e12, 2),
+        zero_masked_padded_tflops=round(flops_pad / (out["zero_masked_ms"] * 1e-3) / 1e12, 2),
         compacted_algorithmic_tflops=round(flops_alg / (out["compacted_ms"] * 1e-3) / 1e12, 2))
     flags = rec.device_status()
     if flags:
@@ -711,6 +847,65 @@ def cpu_baseline(inp, tokens, target_s=15.0):
             "seconds": round(dt, 3), "host": cpu_model()}
 
 
+CPU_STEPS = ("route_stats", "score", "select", "compact", "dgrad", "wgrad")
+BLAS_THREAD_VARS = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS",
+                    "GOTO_NUM_THREADS", "VECLIB_MAXIMUM_THREADS")
+
+
+def cpu_steps_child(workload, tokens, runs=3):
+    """Run in a child process whose BLAS thread count its environment fixed:
+    each step of the oracle timed alone on a token slice (one warm-up, then
+    `runs` timed runs; the median is reported)."""
+    import oracle as O
+    from workloads import generate, get_workload
+
+    inp = token_slice(generate(get_workload(workload)), tokens)
+    w = inp.workload
+    st = O.route_stats(inp.logits, inp.expert_idx, w.E, w.cf, w.rho)
+    R = O.score(inp.g, inp.phi, inp.alpha, w.k)
+    so, ids = O.select(R, inp.expert_idx, w.E, st["quota"])
+    steps = {
+        "route_stats": lambda: O.route_stats(inp.logits, inp.expert_idx, w.E, w.cf, w.rho),
+        "score": lambda: O.score(inp.g, inp.phi, inp.alpha, w.k),
+        "select": lambda: O.select(R, inp.expert_idx, w.E, st["quota"]),
+        "compact": lambda: O.compact(inp.g, inp.phi, inp.alpha, ids, w.k),
+        "dgrad": lambda: O.grouped_dgrad(inp.g, inp.W, inp.alpha, so, ids, w.E, w.k),
+        "wgrad": lambda: O.grouped_wgrad(inp.g, inp.phi, inp.alpha, so, ids, w.E, w.k),
+    }
+    out = {}
+    for name in CPU_STEPS:
+        steps[name]()
+        times = []
+        for _ in range(runs):
+            t0 = time.perf_counter()
+            steps[name]()
+            times.append(time.perf_counter() - t0)
+        out[name] = round(statistics.median(times), 5)
+    retained = int(so[-1])
+    total = sum(out[n] for n in CPU_STEPS if n != "route_stats")
+    return {"seconds": out, "retained_pairs": retained, "routed_pairs": w.N, "tokens": w.T,
+            "value": round(retained / total, 1), "unit": UNIT}
+
+
+def cpu_per_step(workload, tokens):
+    """The oracle per step at one thread and at all host cores, each in a child
+    process with the BLAS thread variables set before numpy loads."""
+    out = {"what": f"fp64 numpy oracle per step on the first {tokens} tokens of {workload}; median of 3 timed runs "
+                   "after 1 warm-up; value = retained pairs over score..wgrad seconds (route stats apart)",
+           "host": cpu_model()}
+    for label, threads in (("threads_1", 1), ("threads_all", cpu_cores())):
+        env = dict(os.environ, **{v: str(threads) for v in BLAS_THREAD_VARS})
+        try:
+            r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-steps-child", "--workload", workload,
+                                "--ref-tokens", str(tokens)], env=env, capture_output=True, text=True, timeout=600)
+            ent = json.loads(r.stdout.strip().splitlines()[-1]) if r.returncode == 0 else {"error": r.stderr[-300:]}
+        except (subprocess.SubprocessError, ValueError, IndexError) as ex:
+            ent = {"error": str(ex)[:300]}
+        ent["threads"] = threads
+        out[label] = ent
+    return out
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return None
@@ -765,6 +960,9 @@ def run_reference(args, rank, world):
 
 def main():
     args = parse()
+    if args.cpu_steps_child:
+        print(json.dumps(cpu_steps_child(args.workload, args.ref_tokens or 4096)))
+        return
     rank, world, local = dist_env()
     if args.impl == "reference":
         res = run_reference(args, rank, world)

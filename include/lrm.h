@@ -253,8 +253,8 @@ LRM_API lrm_status lrm_grouped_dgrad(lrm_ctx* ctx, const uint16_t* delta_c, cons
 
 /*
  * The inverse mapping (LRMoE sec. 1 and 3.3; Alg. 1, ScatterWithZeros;
- * sec. 3.4: retained results go back to their original positions, zeros are
- * restored before the next dense-layer boundary), in two calls:
+ * sec. 3.4: kept rows return to their pairs' slots, dropped pairs' slots are
+ * zero-filled for the next dense layer), in two calls:
  *
  * lrm_grouped_dgrad_scatter: step 5a with the rows written through the
  * selection: the input-gradient row of retained pair u = sel_ids[r] goes to
@@ -276,8 +276,8 @@ LRM_API lrm_status lrm_zero_dropped_rows(lrm_ctx* ctx, const int32_t* sel_offset
                                  void* stream);
 
 /*
- * FC1 side of the expert backward on the retained pairs (LRMoE sec. 3.4:
- * compaction reduces the row dimension of all four expert-backward GEMMs).
+ * FC1 side of the expert backward on the retained pairs (LRMoE sec. 3.4: the
+ * compacted row count sizes all four expert-backward GEMMs).
  * The activation is read as SwiGLU: FC1 gives [a | b] (gate, up; width 2I)
  * per pair and phi = silu(a) * b, silu(a) = a / (1 + exp(-a)).  The FC1 GEMMs
  * are lrm_grouped_dgrad / lrm_grouped_wgrad with the dimensions relabelled:

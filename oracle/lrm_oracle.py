@@ -9,8 +9,9 @@ Sources (cited by page title and the section / equation / figure):
 
 * "LRMoE: Demand-Side Load Re-Calibration for Efficient MoE Training on
   Memory-Constrained Nodes" (Hu et al.), called LRMoE below:
-  sec. 3.1 (quotas K_e with rho = sum K_e / N; compaction in a consistent pair
-  order with counts and prefix offsets), sec. 3.2 Prop. 3.1 eq. (1)-(3) (the
+  sec. 3.1 (quotas K_e with rho = sum K_e / N; compaction keeps the pairs in
+  one fixed order and is described by per-expert counts and their prefix
+  sums), sec. 3.2 Prop. 3.1 eq. (1)-(3) (the
   Load Recalibration Metric), sec. 3.3 Alg. 1 (score, per-expert
   TopK, compaction, packed expert backward), Fig. 4 and sec. 3.4 (variable-M
   grouped GEMMs without padding; equivalence with zero-masking), appendix 7.1
@@ -151,8 +152,8 @@ def route_stats(logits, expert_idx, E: int, cf=Fraction(5, 4), rho=Fraction(3, 4
     * quotas Q_e = ceil(rho * min(n_e, C)) unless ``quota`` is given, with
       realised rate sum Q / N (LRMoE sec. 3.1: rho = sum K_e / N);
     * a bucket of pair ids grouped by expert (ascending u inside an expert)
-      and its prefix offsets, the "counts and prefix offsets" of LRMoE
-      sec. 3.3.
+      and its prefix offsets: the per-expert counts and their prefix sums
+      that LRMoE sec. 3.3 describes compaction with.
     """
     expert_idx = np.asarray(expert_idx)
     T, k = expert_idx.shape
@@ -393,8 +394,8 @@ def grouped_dgrad(g_bits, W_bits, alpha, sel_offsets, sel_ids, E: int, k: int, e
 
 def scatter_with_zeros(rows, sel_ids, N: int) -> np.ndarray:
     """The inverse mapping of LRMoE (sec. 1 and 3.3; Alg. 1,
-    ScatterWithZeros; sec. 3.4: retained results go back to their original
-    positions and zeros are restored before the next dense-layer boundary):
+    ScatterWithZeros; sec. 3.4: kept rows return to their pairs' slots and
+    dropped pairs' slots hold zeros for the next dense layer):
     row r of `rows` (the r-th retained pair in the compacted order) goes to
     row sel_ids[r] of an [N, width] array whose other rows are zero."""
     rows = np.asarray(rows)
@@ -405,9 +406,9 @@ def scatter_with_zeros(rows, sel_ids, N: int) -> np.ndarray:
 
 
 # ---------------------------------------------------------------------------
-# FC1 and its activation on the retained pairs (LRMoE sec. 3.4: compaction
-# reduces the row dimension of all four expert-backward GEMMs, the FC1 and
-# FC2 data- and weight-gradient operations).  The pages do not name the
+# FC1 and its activation on the retained pairs (LRMoE sec. 3.4: the
+# compacted row count sizes all four expert-backward GEMMs, the input- and
+# weight-gradient products of FC1 and FC2).  The pages do not name the
 # activation; it is read as SwiGLU: FC1 maps the expert input x_t to
 # [a_u ; b_u] = W1_e x_t (W1_e is [2I, h], gate rows first), and the FC2
 # input is phi_u = silu(a_u) * b_u with silu(a) = a / (1 + exp(-a)).
