@@ -244,7 +244,7 @@ class Recalibration:
 class StepGraph:
     """The whole step (route stats through the weight gradient) captured once
     as a CUDA graph over fixed device buffers: one launch per step instead of
-    nine library calls, so the host issues nothing per kernel.  The graph
+    one call per kernel, so the host issues nothing per kernel.  The graph
     reads the tensors it was captured with; a caller feeds a new batch by
     writing into them (``copy_``) before ``replay``.  The first, eager run
     does each kernel's one-time set-up (function attributes, occupancy), which

@@ -38,8 +38,8 @@ METRIC = "retained pairs/s through score->select->compact->grouped GEMM"
 UNIT = "pairs/s"
 KERNELS = ("route_stats", "score", "select", "compact", "dgrad", "wgrad")
 # kernels of one step: route stats 3 (count, finalize, scatter), score 1,
-# select 2 (gather, select), compact 1, dgrad 1, wgrad 1
-LAUNCHES_PER_STEP = 9
+# select 1 (one cluster of CTAs per expert), compact 1, dgrad 1, wgrad 1
+LAUNCHES_PER_STEP = 8
 
 
 def parse():
