@@ -181,12 +181,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CfgPair<BN>::THREADS
   const int total_tiles = E * per_expert;
 
   // Schedule: the pair tiles of all experts, heaviest expert first, cut into
-  // blocks of one tile per pair.  Rounds alternate between the heavy front
-  // and the light back of that list (blocks 0, last, 1, last - 1, ...), so the
-  // long K loops of heavy tiles overlap the dW stores of light ones, and the
-  // tiles of one expert still run side by side (their operands are shared
-  // through L2).  Within a block the deal is a snake (forward for even
-  // blocks, backward for odd ones), which balances the ragged K loops.
+  // rounds of one tile per pair, dealt as a snake (forward in even rounds,
+  // backward in odd ones), which balances the ragged K loops; the tiles of
+  // one expert run side by side (their operands are shared through L2).
+  // Measured against rounds that alternate between the heavy front and the
+  // light back of the list: equal on the Qwen3-shaped layer, 2-3.5 % faster
+  // on the GLM-4.5-, DeepSeek-V2-shaped and 131k-token layers (back-to-back
+  // light tiles let the ring run several tiles ahead).
   for (int e = tid; e < E; e += C::THREADS) {
     int st, ln;
     segment(sel_offsets, e, max_rows, st, ln);
@@ -232,10 +233,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CfgPair<BN>::THREADS
     raise_flag(status, LRM_ERR_TIMEOUT);
   };
   const int nblocks = (total_tiles + npairs - 1) / npairs;
-  auto tile_of = [&](int round) {
-    const int b = (round & 1) ? nblocks - 1 - (round >> 1) : (round >> 1);
-    return b * npairs + ((b & 1) ? npairs - 1 - pair : pair);
-  };
+  auto tile_of = [&](int round) { return round * npairs + ((round & 1) ? npairs - 1 - pair : pair); };
   auto decode = [&](int tile, int& e, int& mt, int& nt) {
     const int slot = tile / per_expert;
     e = s_order[slot];
