@@ -107,38 +107,48 @@ __global__ void __launch_bounds__(RS_THREADS) rs_count(const float* __restrict__
     if (e >= 0) atomicAdd(&hist[e], 1);
   }
 
-  // softmax over all E experts, one warp per token; lane owns experts lane + 32 i
+  // softmax over all E experts, one warp per token; lane owns experts lane + 32 i.
+  // DEPTH tokens of a warp are loaded together (a warp walks several tokens,
+  // and one load in flight left it waiting on DRAM once per token)
+  constexpr int DEPTH = VPL <= 4 ? 4 : (VPL <= 8 ? 2 : 1);
   float acc[VPL];
 #pragma unroll
   for (int i = 0; i < VPL; ++i) acc[i] = 0.f;
-  int t = tok0 + warp;
-  float cur[VPL];
-  if (t < tok1) load_logits<VPL>(logits + static_cast<size_t>(t) * E, E, lane, cur);
-  for (; t < tok1; t += RS_WARPS) {
-    float nxt[VPL];
-    const int tn = t + RS_WARPS;
-    if (tn < tok1) load_logits<VPL>(logits + static_cast<size_t>(tn) * E, E, lane, nxt);
-    float mx = -INFINITY;
+  for (int t0 = tok0 + warp; t0 < tok1; t0 += DEPTH * RS_WARPS) {
+    float cur[DEPTH][VPL];
 #pragma unroll
-    for (int i = 0; i < VPL; ++i) mx = fmaxf(mx, cur[i]);
+    for (int d = 0; d < DEPTH; ++d) {
+      const int t = t0 + d * RS_WARPS;
+      if (t < tok1) {
+        load_logits<VPL>(logits + static_cast<size_t>(t) * E, E, lane, cur[d]);
+      } else {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    // the CUDA fast exponential (cur - mx <= 0, where its error is a few ulp
-    // of each term) and one reciprocal per token: P_e is a mean over tokens,
-    // held to 1e-5 relative against the fp64 oracle
-    float s = 0.f;
-#pragma unroll
-    for (int i = 0; i < VPL; ++i) {
-      cur[i] = (lane + 32 * i < E) ? __expf(cur[i] - mx) : 0.f;
-      s += cur[i];
+        for (int i = 0; i < VPL; ++i) cur[d][i] = -INFINITY;
+      }
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    const float inv = 1.f / s;
+    for (int d = 0; d < DEPTH; ++d) {
+      if (t0 + d * RS_WARPS >= tok1) break;
+      float mx = -INFINITY;
 #pragma unroll
-    for (int i = 0; i < VPL; ++i) acc[i] += cur[i] * inv;
+      for (int i = 0; i < VPL; ++i) mx = fmaxf(mx, cur[d][i]);
 #pragma unroll
-    for (int i = 0; i < VPL; ++i) cur[i] = nxt[i];
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      // the CUDA fast exponential (cur - mx <= 0, where its error is a few ulp
+      // of each term) and one reciprocal per token: P_e is a mean over tokens,
+      // held to 1e-5 relative against the fp64 oracle
+      float s = 0.f;
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) {
+        cur[d][i] = (lane + 32 * i < E) ? __expf(cur[d][i] - mx) : 0.f;
+        s += cur[d][i];
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+      const float inv = 1.f / s;
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) acc[i] += cur[d][i] * inv;
+    }
   }
 #pragma unroll
   for (int i = 0; i < VPL; ++i) {
