@@ -227,10 +227,31 @@ class Recalibration:
         else:
             self.wgrad(stream)
 
-    def run(self, logits, expert_idx, g, phi, alpha, W, stream=None, dw_bf16: bool = False):
-        """The whole path, enqueued on one stream."""
-        self.route_stats(logits, expert_idx, stream)
-        self.backward_steps(g, phi, alpha, W, stream, dw_bf16=dw_bf16)
+    def run(self, logits, expert_idx, g, phi, alpha, W, stream=None, dw_bf16: bool = False, side_stream=None):
+        """The whole path, enqueued on one stream.  Route statistics and score
+        read disjoint inputs, so with `side_stream` (a torch stream; `stream`
+        must then be a torch stream or None) route statistics run on it beside
+        score, and select waits for both."""
+        if side_stream is None:
+            self.route_stats(logits, expert_idx, stream)
+            self.backward_steps(g, phi, alpha, W, stream, dw_bf16=dw_bf16)
+            return
+        main = torch.cuda.current_stream(self.device) if stream is None else stream
+        fork = torch.cuda.Event()
+        fork.record(main)
+        side_stream.wait_event(fork)
+        self.route_stats(logits, expert_idx, side_stream)
+        self.score(g, phi, alpha, main)
+        join = torch.cuda.Event()
+        join.record(side_stream)
+        main.wait_event(join)
+        self.select(main)
+        self.compact(g, phi, alpha, main)
+        self.dgrad(W, main)
+        if dw_bf16:
+            self.wgrad_bf16(main)
+        else:
+            self.wgrad(main)
 
     def summary(self) -> dict:
         raw = bytes(self.buf.summary.cpu().numpy().tobytes())
@@ -244,24 +265,27 @@ class Recalibration:
 class StepGraph:
     """The whole step (route stats through the weight gradient) captured once
     as a CUDA graph over fixed device buffers: one launch per step instead of
-    one call per kernel, so the host issues nothing per kernel.  The graph
-    reads the tensors it was captured with; a caller feeds a new batch by
-    writing into them (``copy_``) before ``replay``.  The first, eager run
-    does each kernel's one-time set-up (function attributes, occupancy), which
-    must not happen inside a capture."""
+    one call per kernel, so the host issues nothing per kernel.  Route
+    statistics form a branch of their own beside score (they read disjoint
+    inputs), joined before select.  The graph reads the tensors it was
+    captured with; a caller feeds a new batch by writing into them
+    (``copy_``) before ``replay``.  The first, eager run does each kernel's
+    one-time set-up (function attributes, occupancy), which must not happen
+    inside a capture."""
 
     def __init__(self, rec: "Recalibration", logits, expert_idx, g, phi, alpha, W, dw_bf16: bool = False):
         self.rec = rec
         self.inputs = dict(logits=logits, expert_idx=expert_idx, g=g, phi=phi, alpha=alpha, W=W)
         dev = rec.device
         side = torch.cuda.Stream(dev)
+        branch = torch.cuda.Stream(dev)  # the route statistics branch
         side.wait_stream(torch.cuda.current_stream(dev))
         self.graph = torch.cuda.CUDAGraph()
         with torch.cuda.stream(side):
-            rec.run(logits, expert_idx, g, phi, alpha, W, stream=side, dw_bf16=dw_bf16)
+            rec.run(logits, expert_idx, g, phi, alpha, W, stream=side, dw_bf16=dw_bf16, side_stream=branch)
             side.synchronize()
             with torch.cuda.graph(self.graph, stream=side):
-                rec.run(logits, expert_idx, g, phi, alpha, W, stream=side, dw_bf16=dw_bf16)
+                rec.run(logits, expert_idx, g, phi, alpha, W, stream=side, dw_bf16=dw_bf16, side_stream=branch)
         torch.cuda.current_stream(dev).wait_stream(side)
 
     def replay(self) -> None:

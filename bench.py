@@ -399,8 +399,8 @@ def run_ours(args, rank, world, local):
                        f"g {w.T * w.h * 2 / 2**20:.0f} MiB; L2 129 MB)"),
             },
             "roofline": top,
-            "launch": "CUDA graph of the whole step (StepGraph.replay); per-kernel times from the same step "
-                      "issued call by call with events between the calls",
+            "launch": "CUDA graph of the whole step (StepGraph.replay; route stats a branch beside score); "
+                      "per-kernel times from the same step issued call by call with events between the calls",
             "eager": {"ms_per_step": round(eager_ms / K, 5), "value": round(retained * K / (eager_ms * 1e-3), 1)},
             "pipeline_frac": round(ideal_s / steps_s, 4),
             "score_select_compact": {
