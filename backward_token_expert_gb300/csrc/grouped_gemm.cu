@@ -633,7 +633,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CfgDgradPair<BNR>::T
     *abort_flag = 1;
     raise_flag(status, LRM_ERR_TIMEOUT);
   };
-  // tile -> expert, row tile nt (over the segment), width tile mt (over I)
+  // tile -> expert, row tile nt (over the segment), width tile mt (over I);
+  // within an expert the row tiles run fastest, so pairs dealt neighbouring
+  // tiles share the same W_e columns (1-4 % faster than width tiles fastest
+  // on the Qwen3-, GLM-4.5- and DeepSeek-V2-shaped layers, measured)
   auto decode = [&](int tile, int& e, int& nt, int& mt) {
     int lo = 0, hi = E - 1;  // last position with s_prefix <= tile
     while (lo < hi) {
@@ -645,8 +648,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CfgDgradPair<BNR>::T
     }
     e = s_order[lo];
     const int rem = tile - s_prefix[lo];
-    nt = rem / tiles_m;
-    mt = rem - nt * tiles_m;
+    const int n_nt = (s_len[e] + BNR - 1) / BNR;
+    mt = rem / n_nt;
+    nt = rem - mt * n_nt;
   };
   // rows of row tile nt that the MMA computes: the remainder rounded up to 32
   // (N of a pair MMA with M = 256 is a multiple of 32)
