@@ -24,7 +24,8 @@
 //  3. classify: per warp, the keys above bin b1 are counted and the keys
 //     inside it kept as candidates (with their slice positions);
 //  4. barrier; every CTA copies all candidates of the cluster and finds the
-//     exact boundary key tau with up to three radix passes (7, 7 and 6 bits),
+//     exact boundary key tau with up to three radix passes (7, 7 and 6 bits,
+//     by one warp),
 //     and how many keys equal to tau are kept (the first ones in pair order,
 //     so ties go to the lower pair index).  A bin kept whole ends the search
 //     early ("key >= bin start").  When a CTA has more candidates than it can
@@ -49,6 +50,7 @@ constexpr int SEL_RB = 128;                // bins of the candidates' 7-bit radi
 constexpr int SEL_GRP = 32;                // bins per group of the 64-bin summary
 constexpr int SEL_BATCH = 16;              // independent loads in flight per thread (gather)
 constexpr int SEL_UNR = 8;                 // keys per lane loaded together in the passes over a slice
+constexpr int SEL_LCAP = SEL_NB / (2 * SEL_W);  // kept (position, row) pairs a warp lists for the id loads
 static_assert(SEL_NB / SEL_CL <= 2 * SEL_T, "each thread scans at most two bins of its CTA's share");
 static_assert(SEL_CL * SEL_CCAP <= SEL_NB, "the histogram's space holds every CTA's candidates");
 static_assert(SEL_WCAP == 64, "a warp moves its candidate region two per lane");
@@ -191,10 +193,12 @@ __device__ void cluster_level(Shared& sh, int nb, int want, uint32_t rank, int& 
 }
 
 // The exact boundary key among the m candidates in sh.hist[0, m) (all in
-// bin b1 of the top 11 bits), by radix passes over 7, 7 and 6 bits.  want:
-// keys to keep among them (1 <= want <= m).  Every thread gets the result.
-__device__ void resolve_candidates(Shared& sh, int m, int b1, int want, uint32_t& tau, int& want_eq, bool& ge) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+// bin b1 of the top 11 bits), by radix passes over 7, 7 and 6 bits, run by
+// one warp (the candidates are few, so the warp's own synchronisation is
+// cheaper than the block's).  want: keys to keep among them (1 <= want <= m).
+__device__ void resolve_candidates_warp(Shared& sh, int m, int b1, int want, uint32_t& tau, int& want_eq,
+                                        bool& ge) {
+  const int lane = threadIdx.x & 31;
   const uint32_t* ck = reinterpret_cast<const uint32_t*>(sh.hist);
   uint32_t pre = static_cast<uint32_t>(b1);
   constexpr int kShift[3] = {13, 6, 0};
@@ -202,36 +206,38 @@ __device__ void resolve_candidates(Shared& sh, int m, int b1, int want, uint32_t
 #pragma unroll
   for (int lv = 0; lv < 3; ++lv) {
     const int shift = kShift[lv], bits = kBits[lv], nb = 1 << bits;
-    if (tid < SEL_RB) sh.scratch[tid] = 0;
-    __syncthreads();
-    for (int i = tid; i < m; i += SEL_T) {
+    for (int b = lane; b < SEL_RB; b += 32) sh.scratch[b] = 0;
+    __syncwarp();
+    for (int i = lane; i < m; i += 32) {
       const uint32_t k = ck[i];
       if ((k >> (shift + bits)) == pre) atomicAdd(&sh.scratch[(k >> shift) & static_cast<uint32_t>(nb - 1)], 1);
     }
-    __syncthreads();
-    if (warp == 0) {
-      // lane l holds bins nb-1-4l .. nb-4-4l (descending)
-      int c[4], sum = 0;
+    __syncwarp();
+    // lane l holds bins nb-1-4l .. nb-4-4l (descending)
+    int c[4], sum = 0;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int b = nb - 1 - 4 * lane - j;
-        c[j] = b >= 0 ? sh.scratch[b] : 0;
-        sum += c[j];
-      }
-      int unused;
-      int a = warp_exclusive_scan(sum, lane, &unused);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        if (a < want && want <= a + c[j]) {
-          sh.res[0] = nb - 1 - 4 * lane - j;
-          sh.res[1] = a;
-          sh.res[2] = c[j];
-        }
-        a += c[j];
-      }
+    for (int j = 0; j < 4; ++j) {
+      const int bb = nb - 1 - 4 * lane - j;
+      c[j] = bb >= 0 ? sh.scratch[bb] : 0;
+      sum += c[j];
     }
-    __syncthreads();
-    const int bin = sh.res[0], above = sh.res[1], cnt = sh.res[2];
+    int unused;
+    int a = warp_exclusive_scan(sum, lane, &unused);
+    int f_bin = -1, f_above = 0, f_cnt = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (a < want && want <= a + c[j]) {
+        f_bin = nb - 1 - 4 * lane - j;
+        f_above = a;
+        f_cnt = c[j];
+      }
+      a += c[j];
+    }
+    const int src = __ffs(__ballot_sync(0xffffffffu, f_bin >= 0)) - 1;
+    const int bin = __shfl_sync(0xffffffffu, f_bin, src);
+    const int above = __shfl_sync(0xffffffffu, f_above, src);
+    const int cnt = __shfl_sync(0xffffffffu, f_cnt, src);
+    __syncwarp();  // every lane has read the bins before the next pass clears them
     pre = (pre << bits) | static_cast<uint32_t>(bin);
     want -= above;
     if (cnt == want) {  // the bin is kept whole
@@ -487,7 +493,18 @@ __global__ void __cluster_dims__(SEL_CL, 1, 1) __launch_bounds__(SEL_T, 8)
                                     static_cast<uint32_t>(r));
       }
       __syncthreads();
-      resolve_candidates(sh, m, b1, want1, tau, want_eq, ge);
+      if (warp == 0) {
+        resolve_candidates_warp(sh, m, b1, want1, tau, want_eq, ge);
+        if (lane == 0) {
+          sh.res[0] = static_cast<int>(tau);
+          sh.res[1] = want_eq;
+          sh.res[2] = ge ? 1 : 0;
+        }
+      }
+      __syncthreads();
+      tau = static_cast<uint32_t>(sh.res[0]);
+      want_eq = sh.res[1];
+      ge = sh.res[2] != 0;
     } else {
       // too many candidates somewhere: two histogram levels over the cluster
       const int nc = cand_ok ? n_cand : len;
@@ -586,8 +603,13 @@ __global__ void __cluster_dims__(SEL_CL, 1, 1) __launch_bounds__(SEL_T, 8)
 
   // place the kept ids of this warp's part in ascending u: a kept key goes to
   // (#kept above tau before it) + min(#equal to tau before it, want_eq).
-  // First the output row of every key replaces the key (-1 when dropped),
-  // then the pair ids of the kept ones are loaded many at a time and stored.
+  // First the output row of every key replaces the key (-1 when dropped) and
+  // the kept ones are listed (slice position, output row) in the warp's
+  // region of the histogram space, which no CTA reads any more; then the
+  // pair ids of the listed keys are loaded all at once and stored (a warp
+  // that keeps more than the region holds loads them in batches instead).
+  int* kept = sh.hist + warp * 2 * SEL_LCAP;
+  int n_kept = 0;
   for (int i0 = w0; i0 < w1; i0 += 32 * SEL_UNR) {
     uint32_t kv[SEL_UNR];
 #pragma unroll
@@ -608,11 +630,32 @@ __global__ void __cluster_dims__(SEL_CL, 1, 1) __launch_bounds__(SEL_T, 8)
       int pos = (gt || (eq && my_eq < want_eq)) ? gtb + __popc(bg & lt_mask) + min(my_eq, want_eq) : -1;
       if (pos >= q_out) pos = -1;
       if (live) K[i] = static_cast<uint32_t>(pos);
+      const unsigned bk = __ballot_sync(0xffffffffu, pos >= 0);
+      const int slot = n_kept + __popc(bk & lt_mask);
+      if (pos >= 0 && slot < SEL_LCAP) {
+        kept[2 * slot] = i;
+        kept[2 * slot + 1] = pos;
+      }
+      n_kept += __popc(bk);
       gtb += __popc(bg);
       eqb += __popc(be);
     }
   }
   __syncwarp();
+  if (n_kept <= SEL_LCAP) {
+    int id[SEL_LCAP / 32], row[SEL_LCAP / 32];
+#pragma unroll
+    for (int j = 0; j < SEL_LCAP / 32; ++j) {
+      const int x = 32 * j + lane;
+      row[j] = x < n_kept ? kept[2 * x + 1] : -1;
+      id[j] = x < n_kept ? __ldg(ids + kept[2 * x]) : 0;
+    }
+#pragma unroll
+    for (int j = 0; j < SEL_LCAP / 32; ++j)
+      if (row[j] >= 0) out[row[j]] = id[j];
+    cluster_wait();
+    return;
+  }
   for (int i0 = w0; i0 < w1; i0 += 32 * SEL_BATCH) {
     int pos[SEL_BATCH], id[SEL_BATCH];
 #pragma unroll
