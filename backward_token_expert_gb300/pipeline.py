@@ -237,6 +237,8 @@ class Recalibration:
             self.backward_steps(g, phi, alpha, W, stream, dw_bf16=dw_bf16)
             return
         main = torch.cuda.current_stream(self.device) if stream is None else stream
+        if not isinstance(main, torch.cuda.Stream) or not isinstance(side_stream, torch.cuda.Stream):
+            raise TypeError("run(side_stream=...) needs torch streams for both branches")
         fork = torch.cuda.Event()
         fork.record(main)
         side_stream.wait_event(fork)
