@@ -172,3 +172,32 @@ def test_gradient_l2_metric_at_full_size():
     R = O.score_metric(O.METRIC_GRAD_L2SQ, inp.g, None, None, w.k, n_pairs=w.N)
     assert np.all(rel_close(gpu["score"], R, SCORE_RTOL, 1e-30))
     check_selection(gpu, inp, st["quota"])
+
+
+def _qwen_inputs():
+    if "qwen" not in _SHARED:
+        _SHARED["qwen"] = generate("qwen3_30b_a3b_T32768_E128_k8_h2048_I768")
+    return _SHARED["qwen"]
+
+
+@pytest.mark.parametrize("pattern", ["all_but_one", "half", "one", "random"])
+def test_selection_with_caller_quotas_at_full_size(pattern):
+    """Per-expert selection of the bench layer under caller quotas that put
+    each expert's boundary elsewhere than the rho rule does: near the lowest
+    score (all but one kept, LRMoE Fig. 4's pattern), at the median (the
+    boundary's top-11-bit bin then holds many keys), at the top (one kept) and
+    at random ranks.  The ids must equal the oracle's selection on the GPU's
+    fp32 scores in full, and the compacted rows its compaction on samples."""
+    inp = _qwen_inputs()
+    w = inp.workload
+    n = np.bincount(inp.expert_idx.reshape(-1), minlength=w.E)
+    rng = np.random.default_rng(99)
+    quota = {"all_but_one": np.maximum(n - 1, 0), "half": (n + 1) // 2, "one": np.minimum(n, 1),
+             "random": rng.integers(0, n + 1)}[pattern].astype(np.int32)
+    gpu = run_gpu(inp, quota=quota)
+    assert gpu["flags"] == 0
+    assert np.array_equal(gpu["quota"], quota)
+    so, ids = check_selection(gpu, inp, quota)
+    assert gpu["sel_offsets"][-1] == quota.sum()
+    rows = np.sort(rng.choice(ids.size, size=min(4096, ids.size), replace=False))
+    check_compaction(gpu, inp, ids, rows)
