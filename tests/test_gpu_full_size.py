@@ -201,3 +201,15 @@ def test_selection_with_caller_quotas_at_full_size(pattern):
     assert gpu["sel_offsets"][-1] == quota.sum()
     rows = np.sort(rng.choice(ids.size, size=min(4096, ids.size), replace=False))
     check_compaction(gpu, inp, ids, rows)
+
+
+def test_run_to_run_bit_identity_at_full_size():
+    """Two runs of the bench layer give the same bits everywhere: no output
+    depends on the order in which blocks or atomics happen to run."""
+    inp = _qwen_inputs()
+    a, b = run_gpu(inp), run_gpu(inp)
+    assert a["flags"] == 0 and b["flags"] == 0
+    for key in ("counts", "offsets", "bucket", "quota", "sel_offsets", "sel_ids", "delta_c", "phi_c", "dphi_c"):
+        assert np.array_equal(a[key], b[key]), key
+    for key in ("P", "f", "score", "alpha_c", "dW"):
+        assert np.array_equal(a[key].view(np.uint32), b[key].view(np.uint32)), key
