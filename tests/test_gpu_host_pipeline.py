@@ -1,12 +1,14 @@
 """HostPipeline (host buffers in, host buffers out, copies overlapping the
 neighbouring batches' compute) gives, for every batch of a sequence, exactly
-the results of the single-stream path on the same inputs."""
+the results of the single-stream path on the same inputs, and on the small
+layer the oracle's selection and GEMMs directly."""
 
 import numpy as np
 import pytest
 import torch
 
-from gpu_common import built_library, need_gpu
+import oracle as O
+from gpu_common import GEMM_RTOL, built_library, need_gpu, rel_fro
 from workloads import generate, get_workload
 
 pytestmark = pytest.mark.gpu
@@ -60,6 +62,23 @@ def test_every_batch_matches_the_single_stream_path(name):
                 assert torch.equal(o["summary"], rec.buf.summary.cpu())
                 assert torch.equal(o["dphi_c"][:rows].view(torch.int16), rec.buf.dphi_c[:rows].cpu().view(torch.int16))
                 assert torch.equal(o["dW"], rec.buf.dW.cpu())
+                if w.N <= 4096:
+                    # and straight against the oracle: selection on this batch's fp32
+                    # scores, then the GEMMs from the original inputs
+                    st = O.route_stats(b.logits, b.expert_idx, w.E, w.cf, w.rho)
+                    score = rec.buf.score[: w.N].cpu().numpy().astype(np.float64)
+                    so, ids = O.select(score, b.expert_idx, w.E, st["quota"])
+                    assert np.array_equal(o["sel_offsets"].numpy(), so)
+                    assert np.array_equal(o["sel_ids"][:rows].numpy(), ids)
+                    ref_dW = O.grouped_wgrad(b.g, b.phi, b.alpha, so, ids, w.E, w.k)
+                    ref_dphi = O.grouped_dgrad(b.g, b.W, b.alpha, so, ids, w.E, w.k)
+                    dphi = o["dphi_c"][:rows].float().numpy().astype(np.float64)
+                    for e in range(w.E):
+                        if so[e + 1] == so[e]:
+                            assert not o["dW"][e].any()
+                            continue
+                        assert rel_fro(o["dW"][e].numpy(), ref_dW[e]) <= GEMM_RTOL, e
+                        assert rel_fro(dphi[so[e]:so[e + 1]], ref_dphi[e]) <= GEMM_RTOL, e
         assert set(OUTPUT_NAMES) == set(outs[0])
     finally:
         rec.close()
