@@ -55,6 +55,7 @@ static_assert(SEL_NB / SEL_CL <= 2 * SEL_T, "each thread scans at most two bins 
 static_assert(SEL_CL * SEL_CCAP <= SEL_NB, "the histogram's space holds every CTA's candidates");
 static_assert(SEL_WCAP == 64, "a warp moves its candidate region two per lane");
 static_assert(SEL_NB == 2 * 32 * SEL_GRP, "warp 0 scans the 64-bin summary two groups per lane");
+static_assert(SEL_T % 32 == 0 && (2 * (SEL_NB / SEL_GRP)) % 32 == 0, "the summary loop runs whole warps");
 
 __device__ __forceinline__ uint32_t score_key(float r) { return __float_as_uint(r) & 0x7FFFFFFFu; }
 
@@ -233,7 +234,9 @@ __device__ void resolve_candidates_warp(Shared& sh, int m, int b1, int want, uin
       }
       a += c[j];
     }
-    const int src = __ffs(__ballot_sync(0xffffffffu, f_bin >= 0)) - 1;
+    // exactly one lane holds the rank; max() only keeps a broken invariant
+    // from turning into a lane or bin index out of range
+    const int src = max(__ffs(__ballot_sync(0xffffffffu, f_bin >= 0)) - 1, 0);
     const int bin = __shfl_sync(0xffffffffu, f_bin, src);
     const int above = __shfl_sync(0xffffffffu, f_above, src);
     const int cnt = __shfl_sync(0xffffffffu, f_cnt, src);
@@ -354,14 +357,15 @@ __global__ void __cluster_dims__(SEL_CL, 1, 1) __launch_bounds__(SEL_T, 8)
       if (lo + i < q_out) out[lo + i] = __ldg(ids + i);
     return;
   }
-  {
-    // 64 groups of 32 bins: thread t sums half of group t / 2
+  // 64 groups of 32 bins: index t of the loop sums half of group t / 2 (whole
+  // warps take part in every iteration, as the shuffle needs)
+  for (int t2 = tid; t2 < 2 * (SEL_NB / SEL_GRP); t2 += SEL_T) {
     int g = 0;
-    const int b0 = (tid >> 1) * SEL_GRP + (tid & 1) * (SEL_GRP / 2);
+    const int b0 = (t2 >> 1) * SEL_GRP + (t2 & 1) * (SEL_GRP / 2);
 #pragma unroll
     for (int j = 0; j < SEL_GRP / 2; ++j) g += sh.hist[b0 + j];
     g += __shfl_xor_sync(0xffffffffu, g, 1);
-    if ((tid & 1) == 0) sh.group[tid >> 1] = g;
+    if ((t2 & 1) == 0) sh.group[t2 >> 1] = g;
   }
 
   // 2. barrier; bin b1 of the q-th largest key, found by warp 0 of every CTA
@@ -385,8 +389,8 @@ __global__ void __cluster_dims__(SEL_CL, 1, 1) __launch_bounds__(SEL_T, 8)
       ga = a + ch;
     }
     const unsigned who = __ballot_sync(0xffffffffu, grp >= 0);
-    const int src = __ffs(who) - 1;
-    grp = __shfl_sync(0xffffffffu, grp, src);
+    const int src = max(__ffs(who) - 1, 0);  // exactly one lane holds the rank
+    grp = max(__shfl_sync(0xffffffffu, grp, src), 0);  // in [0, 63]: the bins read below stay in range
     ga = __shfl_sync(0xffffffffu, ga, src);
     // lane l holds bin (grp + 1) * 32 - 1 - l of the group (descending)
     const int bin = (grp + 1) * SEL_GRP - 1 - lane;
