@@ -368,12 +368,8 @@ LRM_API lrm_status lrm_compact_padded(lrm_ctx* ctx, const uint16_t* delta_c, con
  *   scratch has to start at zero and stale contents of an earlier call are
  *   harmless.
  * - Every call looks up the array's device address with the device current
- *   (host-side, no device work).  A call made while `stream` is being
- *   captured into a CUDA graph reuses the address found by the last call on
- *   that device outside a capture: make one call before capturing, and one
- *   more after any reset of the device (cudaDeviceReset) before capturing
- *   again.  A capture whose first call on the device is this one fails with
- *   LRM_ERR_CUDA.
+ *   (host-side, no device work), so a call after a reset of the device
+ *   (cudaDeviceReset) finds the array the module was loaded with again.
  * - All calls share the one array, so calls that may overlap on the GPU
  *   (different streams without ordering between them) race; serialise them.
  * The paper has no counterpart of this entry point.
