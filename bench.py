@@ -251,6 +251,39 @@ def per_kernel_times(rec, d, K):
     return per, eager_ms
 
 
+def graph_kernel_times(rec, d, n=20, reps=3):
+    """Per-kernel time (ms) without host launch cost: n back-to-back calls of
+    one step's kernel captured in a CUDA graph, replayed `reps` times after a
+    warm replay.  Back-to-back calls find their small inputs in L2, so these
+    are a lower bound for the latency-bound kernels' time inside the step."""
+    import torch
+
+    calls = dict(route_stats=lambda s: rec.route_stats(d["logits"], d["expert_idx"], s),
+                 score=lambda s: rec.score(d["g"], d["phi"], d["alpha"], s), select=lambda s: rec.select(s),
+                 compact=lambda s: rec.compact(d["g"], d["phi"], d["alpha"], s),
+                 dgrad=lambda s: rec.dgrad(d["W"], s), wgrad=lambda s: rec.wgrad(s))
+    out = {}
+    for name in KERNELS:
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(graph, stream=side):
+                for _ in range(n):
+                    calls[name](side)
+        torch.cuda.current_stream().wait_stream(side)
+        graph.replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            graph.replay()
+        e1.record()
+        e1.synchronize()
+        out[name] = round(e0.elapsed_time(e1) / (reps * n), 5)
+        del graph
+    return out
+
+
 def kernel_table(w, retained, active, per, pk):
     """Per-kernel mean time, percentiles, share of the step and roofline."""
     work = algorithmic_work(w, retained, active)
@@ -353,6 +386,7 @@ def run_ours(args, rank, world, local):
 
     # per-kernel times: the same step issued call by call, events between the calls
     per, eager_ms = per_kernel_times(rec, d, K)
+    in_graph = graph_kernel_times(rec, d) if rank == 0 else None
     flags = rec.device_status()
     if flags:
         raise RuntimeError(f"device status flags {flags:#x} after the timed steps")
@@ -415,6 +449,8 @@ def run_ours(args, rank, world, local):
                 "value": round(retained / excl_rs_s, 1), "unit": UNIT,
                 "route_stats_ms": kernels["route_stats"]["ms"]},
             "kernels": kernels,
+            "kernels_in_graph_ms": dict(in_graph, what="each kernel alone, 20 back-to-back calls captured in one "
+                                        "CUDA graph: no host launch cost, small inputs warm in L2"),
             "gpu_launches": LAUNCHES_PER_STEP * K,
             "host_s": round(t_host, 4),
             "clocks": sampler.summary() if sampler else None,
