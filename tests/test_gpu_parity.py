@@ -206,3 +206,14 @@ def test_large_experts_sampled_bracket_and_fallback(T, E, mode, seed):
         inp.g[:] = inp.g[rng.integers(0, 3, size=inp.g.shape[0])]
         inp.alpha[:] = np.float32(0.25)
     full_check(inp)
+
+
+@pytest.mark.parametrize("T,E,k,h,I,rho", [(1, 1, 1, 8, 8, Fraction(1)), (3, 4, 4, 16, 8, Fraction(3, 4)),
+                                           (100, 2, 2, 8, 8, Fraction(1, 2)), (300, 32, 32, 64, 40, Fraction(3, 5)),
+                                           (2000, 1, 1, 40, 24, Fraction(1, 3))])
+def test_extreme_shapes(T, E, k, h, I, rho):
+    """A single token, a single expert, every token routed to every expert
+    (k = E, up to the ABI's k = 32), the narrowest rows (h = I = 8) and
+    rows that are no multiple of the 64-column swizzle atom."""
+    inp = custom_inputs(T=T, E=E, k=k, h=h, I=I, s=0.5, rho=rho, seed=T + E + k)
+    full_check(inp)
