@@ -168,6 +168,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CfgPair<BN>::THREADS
   __shared__ uint32_t s_tmem_base;
   __shared__ int s_abort;
   __shared__ int s_len[MAX_E];
+  __shared__ int s_start[MAX_E];  // segment bounds, so no role reads sel_offsets per tile
   __shared__ uint16_t s_order[MAX_E];  // experts by descending retained rows (ties: lower id)
   static_assert(C::STAGES <= 32, "tail parities are kept in one 32-bit mask");
 
@@ -192,6 +193,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CfgPair<BN>::THREADS
     int st, ln;
     segment(sel_offsets, e, max_rows, st, ln);
     s_len[e] = ln;
+    s_start[e] = st;
   }
   __syncthreads();
   for (int e = tid; e < E; e += C::THREADS) {
@@ -255,8 +257,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CfgPair<BN>::THREADS
         if (tile >= total_tiles) continue;
         int e, mt, nt;
         decode(tile, e, mt, nt);
-        int start, len;
-        segment(sel_offsets, e, max_rows, start, len);
+        const int start = s_start[e], len = s_len[e];
         const int nkb = (len + C::BKS - 1) / C::BKS;
         for (int kb = 0; kb < nkb; ++kb, ++it) {
           const uint32_t s = it % C::STAGES;
@@ -311,8 +312,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CfgPair<BN>::THREADS
       if (tile >= total_tiles) continue;
       int e, mt, nt;
       decode(tile, e, mt, nt);
-      int start, len;
-      segment(sel_offsets, e, max_rows, start, len);
+      const int start = s_start[e], len = s_len[e];
       const int nkb = (len + C::BKS - 1) / C::BKS;
       if (nkb == 0) continue;
       const uint32_t acc = acc_it & 1u;
@@ -378,8 +378,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CfgPair<BN>::THREADS
       if (tile >= total_tiles) continue;
       int e, mt, nt;
       decode(tile, e, mt, nt);
-      int start, len;
-      segment(sel_offsets, e, max_rows, start, len);
+      const int start = s_start[e], len = s_len[e];
       const int nkb = (len + C::BKS - 1) / C::BKS;
       if (nkb == 0) continue;
       it += nkb - 1;  // full blocks need no fixing
@@ -433,8 +432,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CfgPair<BN>::THREADS
       decode(tile, e, mt, nt);
       const int row_w = mt * 256 + static_cast<int>(rank) * 128 + q * 32;  // first dW row of this warp
       OutT* obase = out + (static_cast<size_t>(e) * h + row_w) * I;
-      int start, len;
-      segment(sel_offsets, e, max_rows, start, len);
+      const int start = s_start[e], len = s_len[e];
       if (len == 0) {
         if (!accumulate) {
           for (int c = 0; c < BN / 2; c += 16) {
