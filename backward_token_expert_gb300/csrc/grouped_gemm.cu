@@ -561,6 +561,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CfgDgradPair<BNR>::T
   __shared__ uint32_t s_tmem_base;
   __shared__ int s_abort;
   __shared__ int s_len[MAX_E];
+  __shared__ int s_start[MAX_E];  // segment bounds, so no role reads sel_offsets per tile
   __shared__ uint16_t s_order[MAX_E];  // experts in schedule order (descending index)
   __shared__ int s_prefix[MAX_E + 1];  // first pair tile of the expert at each position of s_order
 
@@ -580,6 +581,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CfgDgradPair<BNR>::T
     int st, ln;
     segment(sel_offsets, e, max_rows, st, ln);
     s_len[e] = ln;
+    s_start[e] = st;
     s_order[E - 1 - e] = static_cast<uint16_t>(e);
   }
   __syncthreads();
@@ -666,8 +668,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CfgDgradPair<BNR>::T
       for (int tile = pair; tile < total_tiles && ok; tile += npairs) {
         int e, nt, mt;
         decode(tile, e, nt, mt);
-        int start, len;
-        segment(sel_offsets, e, max_rows, start, len);
+        const int start = s_start[e], len = s_len[e];
         const int half = tile_rows(len, nt) / 2;
         const int xa = mt * 256 + static_cast<int>(rank) * 128;
         const int yb = start + nt * BNR + static_cast<int>(rank) * half;
@@ -705,8 +706,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CfgDgradPair<BNR>::T
     for (int tile = pair; tile < total_tiles && ok; tile += npairs) {
       int e, nt, mt;
       decode(tile, e, nt, mt);
-      int start, len;
-      segment(sel_offsets, e, max_rows, start, len);
+      const int start = s_start[e], len = s_len[e];
       const uint32_t idesc = idesc_bf16_f32(256, static_cast<uint32_t>(tile_rows(len, nt)), 1u, 0u);
       const uint32_t acc = acc_it & 1u;
       const uint32_t aph = (acc_it >> 1) & 1u;
@@ -761,8 +761,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CfgDgradPair<BNR>::T
     for (int tile = pair; tile < total_tiles; tile += npairs) {
       int e, nt, mt;
       decode(tile, e, nt, mt);
-      int start, len;
-      segment(sel_offsets, e, max_rows, start, len);
+      const int start = s_start[e], len = s_len[e];
       const int n_cols = tile_rows(len, nt);
       const int rows_valid = len - nt * BNR;  // rows of this tile inside the segment
       const uint32_t acc = acc_it & 1u;
