@@ -23,16 +23,17 @@
 //     rank, then sums those 32 bins over the CTAs;
 //  3. classify: per warp, the keys above bin b1 are counted and the keys
 //     inside it kept as candidates (with their slice positions);
-//  4. barrier; every CTA copies all candidates of the cluster and finds the
-//     exact boundary key tau with up to three radix passes (7, 7 and 6 bits,
-//     by one warp),
-//     and how many keys equal to tau are kept (the first ones in pair order,
-//     so ties go to the lower pair index).  A bin kept whole ends the search
-//     early ("key >= bin start").  When a CTA has more candidates than it can
-//     hold, the cluster sums two more histogram levels (bits 19-9, 8-0);
+//  4. barrier; every CTA copies all candidates of the cluster and one warp
+//     finds the exact boundary key tau with up to three radix passes (7, 7
+//     and 6 bits) and how many keys equal to tau are kept (the first ones in
+//     pair order, so ties go to the lower pair index).  A bin kept whole ends
+//     the search early ("key >= bin start").  When a CTA has more candidates
+//     than it can hold, the cluster sums two more histogram levels (bits 19-9,
+//     8-0);
 //  5. barrier; per-warp counts of kept keys, a prefix over the cluster's
-//     CTAs and then the warps, and each warp writes the pair ids of its kept
-//     keys in ascending u.
+//     CTAs and then the warps; each warp lists its kept keys (slice position,
+//     output row), loads their pair ids in one round and writes them in
+//     ascending u.
 // No global atomics and no zeroed workspace.
 #include "lrm_internal.cuh"
 
