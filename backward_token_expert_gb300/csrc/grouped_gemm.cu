@@ -312,7 +312,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CfgPair<BN>::THREADS
       if (tile >= total_tiles) continue;
       int e, mt, nt;
       decode(tile, e, mt, nt);
-      const int start = s_start[e], len = s_len[e];
+      const int len = s_len[e];
       const int nkb = (len + C::BKS - 1) / C::BKS;
       if (nkb == 0) continue;
       const uint32_t acc = acc_it & 1u;
@@ -378,7 +378,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CfgPair<BN>::THREADS
       if (tile >= total_tiles) continue;
       int e, mt, nt;
       decode(tile, e, mt, nt);
-      const int start = s_start[e], len = s_len[e];
+      const int len = s_len[e];
       const int nkb = (len + C::BKS - 1) / C::BKS;
       if (nkb == 0) continue;
       it += nkb - 1;  // full blocks need no fixing
@@ -432,7 +432,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CfgPair<BN>::THREADS
       decode(tile, e, mt, nt);
       const int row_w = mt * 256 + static_cast<int>(rank) * 128 + q * 32;  // first dW row of this warp
       OutT* obase = out + (static_cast<size_t>(e) * h + row_w) * I;
-      const int start = s_start[e], len = s_len[e];
+      const int len = s_len[e];
       if (len == 0) {
         if (!accumulate) {
           for (int c = 0; c < BN / 2; c += 16) {
@@ -727,7 +727,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(CfgDgradPair<BNR>::T
     for (int tile = pair; tile < total_tiles && ok; tile += npairs) {
       int e, nt, mt;
       decode(tile, e, nt, mt);
-      const int start = s_start[e], len = s_len[e];
+      const int len = s_len[e];
       const uint32_t idesc = idesc_bf16_f32(256, static_cast<uint32_t>(tile_rows(len, nt)), 1u, 0u);
       const uint32_t acc = acc_it & 1u;
       const uint32_t aph = (acc_it >> 1) & 1u;
