@@ -39,7 +39,7 @@ constexpr int MAX_E = 1024;
 // wgrad on CTA pairs: dW_e [h, I] in 256 x BN output tiles, one per cluster of
 // two CTAs.  CTA r of a pair loads rows [128r, 128r + 128) of the tile's M
 // (= h) range of delta_c^T and columns [r BN/2, (r+1) BN/2) of phi_c into its
-// own 6-stage ring (32 KiB per stage); the even CTA issues the M = 256
+// own 4-stage ring (96 K rows, 48 KiB per stage); the even CTA issues the M = 256
 // tcgen05.mma.cta_group::2, which reads both CTAs' shared memory, so each B
 // byte crosses L2 once per pair.  Each CTA's TMEM holds its 128 rows x BN.
 //   warp 0   TMA producer of the CTA's halves.  Full K blocks: both CTAs'
@@ -52,8 +52,9 @@ constexpr int MAX_E = 1024;
 //            barriers (idle in the odd CTA)
 //   warps 2-9 epilogue of the CTA's own 128 rows, two warps per TMEM lane
 //            quarter (each takes half of the BN columns; TMEM chunks are
-//            prefetched one ahead), TMA tensor stores, then release the
-//            accumulator on the even CTA's barrier (16 arrivals)
+//            prefetched one ahead), a shuffle transpose of 16-byte quads so
+//            that each store instruction writes 8 rows x 64 bytes, then
+//            release the accumulator on the even CTA's barrier (16 arrivals)
 //   warp 10  tail fixer: waits for the CTA's own tail load, zeroes the rows
 //            of its halves that lie past the expert's segment (the MMA reads
 //            whole 16-row K steps) and arrives on the even CTA's full barrier

@@ -9,8 +9,9 @@
 //   rs_count    one block per contiguous chunk of tokens: the chunk's expert
 //               ids are staged in shared memory (validated there), counted
 //               with shared-memory atomics, and the softmax of each token
-//               (one warp per token, the next token's logits prefetched) is
-//               summed per warp in registers, then per block in a fixed order;
+//               (a warp takes up to four tokens at a time, their logits
+//               loaded together) is summed per warp in registers, then per
+//               block in a fixed order;
 //   rs_rows     one warp per expert row of the expert-major workspace: n_e,
 //               P_e, f_e, the quota, and per-(expert, block) bucket bases
 //               relative to the expert's start (loads issued eight at a time);
